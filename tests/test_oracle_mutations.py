@@ -1,0 +1,57 @@
+"""Plant plausible mistakes in copies of the oracle and check a pin fails.
+
+Each mutation rewrites one expression of pa_oracle.c (a dropped term, a wrong
+sign, a wrong index, a swapped operand), compiles the copy into a temporary
+directory on the CPU, and runs the pin battery against it.  A mutation that no
+pin notices would mean the pins could not tell a broken oracle from a correct
+one.
+"""
+import os
+
+import pytest
+
+import oracle
+from pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
+
+MUTATIONS = {
+    "drop_scale": ("weights[t] = scale * dot;", "weights[t] = dot;"),
+    "softmax_sign": ("exp(weights[t] - max_score)", "exp(max_score - weights[t])"),
+    "no_normalisation": ("double w = weights[t] / total;", "double w = weights[t];"),
+    "offset_shift": ("int offset = t % block_size;", "int offset = (t + 1) % block_size;"),
+    "logical_block": ("max_blocks_per_seq + t / block_size];",
+                      "max_blocks_per_seq + (t / block_size) / 2];"),
+    "k_from_v": ("K[(size_t)t * head_dim + d] = oracle_half_to_double(k_cache[at]);",
+                 "K[(size_t)t * head_dim + d] = oracle_half_to_double(v_cache[at]);"),
+    "q_wrong_head": ("qd[d] = oracle_half_to_double(q[(size_t)pair * head_dim + d]);",
+                     "qd[d] = oracle_half_to_double(q[(size_t)s * head_dim + d]);"),
+    "head_offset_transposed": ("size_t at = cache_index(phys, h, offset, d,",
+                               "size_t at = cache_index(phys, offset % num_heads, h % block_size, d,"),
+    "drop_last_token": ("weights[t] = exp(weights[t] - max_score);\n            total += weights[t];",
+                        "weights[t] = (t + 1 < ctx) ? exp(weights[t] - max_score) : 0.0;\n            total += weights[t];"),
+    "half_bias": ("exponent - 25);", "exponent - 24);"),
+    "half_subnormal": ("ldexp((double)fraction, -24);", "ldexp((double)fraction, -25);"),
+    "reshape_offset": ("int offset = slot % block_size;\n        for (int h = 0; h < num_heads; ++h) {",
+                       "int offset = (slot + 1) % block_size;\n        for (int h = 0; h < num_heads; ++h) {"),
+    "reshape_skips_zero": ("if (slot < 0)\n            continue;", "if (slot <= 0)\n            continue;"),
+    "reshape_k_only": ("v_cache[dst] = v[src];", "v_cache[dst] = k[src];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    text = open(SRC, encoding="utf-8").read()
+    assert text.count(old) == 1, f"mutation {name} no longer matches the oracle source"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new), encoding="utf-8")
+    lib = oracle.load(path=str(tmp_path / "libmutant.so"), src=str(src))
+    caught = []
+    for pin_name, fn in PINS:
+        try:
+            fn(lib)
+        except (AssertionError, oracle.OracleError, FloatingPointError):
+            caught.append(pin_name)
+            break
+    assert caught, f"no pin notices mutation {name}"

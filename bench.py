@@ -1,0 +1,389 @@
+"""Benchmark: one decode step of paged attention on GB300.
+
+A step is the whole hot path on one batch: reshape_and_cache of the batch's
+new tokens, then decode over every sequence's paged K/V history.  The default
+workload is the LLaMA-7B-shaped layer (64 sequences, 32 heads, head_dim 128,
+16-token blocks, contexts uniform in [128, 2048], shuffled block placement,
+64 new tokens), with seeded synthetic fp16 N(0, 1) inputs.
+
+Prints one JSON line.  `value` is KV GB/s of the step (algorithmic bytes: K
+and V of every context token, q, the output, the table entries used, the
+context lengths and the new tokens' K/V in and out, divided by the step time,
+device-timed with inputs resident in HBM).  The `roofline` object covers the
+dominant kernel (decode) against the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "pa_decode KV GB/s and % of GB300 HBM peak; decode tokens/s (seq·layer/s)"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ("paged_kv_cache_269_gb300/csrc/pa_decode.cu",
+                  "paged_kv_cache_269_gb300/csrc/pa_device.cuh")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", default="llama7b_b64", choices=workloads.WORKLOADS)
+    p.add_argument("--partition-tokens", type=int, default=0)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="CPU work the oracle baseline leg runs for (bounded sample)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+def step_bytes(case):
+    return workloads.decode_algorithmic_bytes(case) + workloads.reshape_algorithmic_bytes(case)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"pa_decode_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path, encoding="utf-8"):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != decode_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch_full_size"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# oracle (CPU) legs
+# ----------------------------------------------------------------------------
+
+def oracle_sample(case, seconds):
+    """Time the oracle, as it stands, on the whole workload (repeated until
+    `seconds` of CPU work have run, at least once)."""
+    import oracle
+    lib = oracle.load()
+    kc, vc = case.k_cache, case.v_cache
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        if case.num_new_tokens:
+            kc, vc = oracle.reshape_and_cache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                              case.slot_mapping, lib=lib)
+        oracle.decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale, lib=lib)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return el / runs, runs, oracle.num_threads(lib)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    case = workloads.make_workload(args.workload)
+    nbytes = step_bytes(case)
+    # each step: one full pass of the oracle over the workload
+    per_step, cores = [], 0
+    for i in range(args.warmup + args.steps):
+        t, _, cores = oracle_sample(case, 0.0)
+        if i >= args.warmup:
+            per_step.append(t)
+    sec = sum(per_step) / len(per_step)
+    value = nbytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(case, args),
+        "tokens_per_s": round(case.num_seqs / sec, 2),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"full {args.workload} step (reshape_and_cache + decode) "
+                                   f"per timed step, fp64 C oracle with OpenMP"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def config_of(case, args):
+    return {"workload": args.workload, "num_seqs": case.num_seqs, "num_heads": case.num_heads,
+            "head_dim": case.head_dim, "block_size": case.block_size,
+            "num_blocks": case.num_blocks, "max_blocks_per_seq": case.max_blocks_per_seq,
+            "total_context_tokens": int(case.context_lens.sum()),
+            "new_tokens": case.num_new_tokens,
+            "l2": "inputs larger than L2 (no flush)" if 2 * case.k_cache.nbytes > L2_BYTES
+            else "inputs smaller than L2",
+            "parallelism": f"dp{args.gpus} (replicas)", "seed": case.seed}
+
+
+# ----------------------------------------------------------------------------
+# native leg
+# ----------------------------------------------------------------------------
+
+def run_native(args, rank, world, local_rank):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.lib()
+    case = workloads.make_workload(args.workload, new_tokens=True)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d = dict(q=t(case.q), k_cache=t(case.k_cache), v_cache=t(case.v_cache),
+             block_tables=t(case.block_tables), context_lens=t(case.context_lens),
+             k_new=t(case.k_new), v_new=t(case.v_new), slot_mapping=t(case.slot_mapping))
+    out = torch.empty(case.q.shape, dtype=torch.float16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    nws = pa.decode_workspace_bytes(case.num_seqs, case.num_heads, case.head_dim,
+                                    case.block_size, case.num_blocks, case.max_blocks_per_seq,
+                                    args.partition_tokens)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    ctr = torch.zeros(pa.decode_counters_bytes(case.num_seqs, case.num_heads) // 4,
+                      dtype=torch.int32, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(ins, ev=None):
+        pa.reshape_and_cache(ins["k_new"], ins["v_new"], d["k_cache"], d["v_cache"],
+                             ins["slot_mapping"], stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.decode(out, ins["q"], d["k_cache"], d["v_cache"], ins["block_tables"],
+                  ins["context_lens"], case.scale, partition_tokens=args.partition_tokens,
+                  workspace=ws, counters=ctr, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step(d)
+    torch.cuda.synchronize(dev)
+    if pa.device_errors(stream=stream):
+        raise RuntimeError("device error during warm-up")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if not args.no_clocks else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        step(d, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    if sampler:
+        sampler.__exit__(None, None, None)
+    step_ms = start.elapsed_time(end) / args.steps
+    decode_ms_each = [a.elapsed_time(b) for a, b in evs]
+    decode_ms = sum(decode_ms_each) / len(decode_ms_each)
+    if pa.device_errors(stream=stream):
+        raise RuntimeError("device error during the timed steps")
+
+    # e2e: per-step inputs from pinned host memory, result read back every step
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(np.ascontiguousarray(getattr(case, k))).pin_memory()
+                for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for k, v in host.items():
+                    dev_in[k].copy_(v, non_blocking=True)
+            step(dev_in)
+            with torch.cuda.stream(stream):
+                out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        if dist:
+            tt = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        e2e = {"value": round(world * step_bytes(case) / e2e_s / 1e9, 3), "unit": UNIT,
+               "ms_per_step": round(e2e_s * 1e3, 4),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if dist:
+        tt = torch.tensor([step_ms, decode_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms, decode_ms = (float(x) for x in tt.tolist())
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    dec_bytes = workloads.decode_algorithmic_bytes(case)
+    achieved = dec_bytes / (decode_ms * 1e-3) / 1e9
+    value = world * step_bytes(case) / (step_ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        sec, runs, cores = oracle_sample(case, args.cpu_seconds)
+        cpu = {"value": round(step_bytes(case) / sec / 1e9, 4), "unit": UNIT, "cores": cores,
+               "kind": "oracle",
+               "sample": f"full {args.workload} step (reshape_and_cache + decode), "
+                         f"{runs} run(s), {sec:.2f} s each"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": config_of(case, args),
+        "tokens_per_s": round(world * case.num_seqs / (step_ms * 1e-3), 1),
+        "pct_of_peak": round(100 * value / peak, 2),
+        "decode_ms": round(decode_ms, 4),
+        "decode_ms_median": round(statistics.median(decode_ms_each), 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "pa_decode", "algorithmic_bytes_per_launch": int(dec_bytes),
+                     "traffic": recorded_traffic(args.workload)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary() if sampler else None,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_native(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

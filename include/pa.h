@@ -1,0 +1,200 @@
+/*
+ * pa.h -- C ABI of libpa: PagedAttention decode on one GB300 (sm_103a).
+ *
+ * The library implements the one data-parallel hot path the pages on vLLM
+ * turn on: for each running sequence, one fp16 query per head attends over
+ * that sequence's K/V history, o = softmax(scale * K q)^T V
+ * ("vLLM 2026 推理引擎全解：从 PagedAttention 到分离式 Prefill", §1.1).  The
+ * history lives in fixed-size KV blocks scattered through device memory and is
+ * reached through a per-sequence block table (logical block -> physical
+ * block); blocks may be shared between sequences with a common prompt prefix
+ * (same page, §2.1 and §2.3; mjmagnets.cn vLLM tutorial, §2.1-§2.2).
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" must point to device memory of the current CUDA
+ *    device (or memory the device can read, such as managed memory); pointers
+ *    marked "host" are read on the host during the call only.
+ *  - The caller owns every buffer.  The library keeps no pointer past the call.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL means the legacy
+ *    default stream) and runs asynchronously: a PA_OK return means the launch
+ *    succeeded, not that the kernel has finished.
+ *  - fp16 tensors are IEEE binary16, row-major and contiguous in the shapes
+ *    given; every fp16 device pointer must be 16-byte aligned.
+ *  - Errors found on the host return a negative pa_status and launch nothing.
+ *    Errors only the device can see (a block-table entry or slot outside the
+ *    pool, a context length outside [0, max_blocks_per_seq * block_size]) are
+ *    recorded in a per-device error word, read with pa_device_errors(); the
+ *    kernels skip the offending access instead of faulting.
+ *  - No call aborts, throws or traps.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_NULL = -1,          /* a required pointer is NULL                    */
+    PA_ERR_SHAPE = -2,         /* a size is negative, zero where it must not be, or overflows */
+    PA_ERR_UNSUPPORTED = -3,   /* head_dim / block_size outside the built variants */
+    PA_ERR_ALIGN = -4,         /* an fp16 pointer is not 16-byte aligned        */
+    PA_ERR_WORKSPACE = -5,     /* workspace or counter buffer missing, too small or misaligned */
+    PA_ERR_CUDA = -6           /* a CUDA runtime call failed; see pa_last_cuda_error() */
+} pa_status;
+
+/* Bits of the per-device error word (pa_device_errors). */
+#define PA_DEVERR_TABLE   0x1u  /* a used block-table entry was outside [0, num_blocks)   */
+#define PA_DEVERR_CONTEXT 0x2u  /* a context length was < 0 or > max_blocks_per_seq * block_size */
+#define PA_DEVERR_SLOT    0x4u  /* a slot_mapping entry was >= num_blocks * block_size      */
+#define PA_DEVERR_TIMEOUT 0x8u  /* an internal pipeline wait gave up (should never happen) */
+
+/* Sizes shared by both calls.
+ *   num_seqs    S: sequences in the decode batch (>= 0)
+ *   num_heads   H: attention heads; K/V heads equal query heads (no grouping)
+ *   head_dim    D: 64, 128 or 256
+ *   block_size  B: tokens per KV block: 8, 16 (the pages' default) or 32
+ *   num_blocks  N: physical blocks in the cache pool (> 0)
+ * Cache layout [N, H, B, D] fp16: element (blk, h, t, d) is at
+ * ((blk * H + h) * B + t) * D + d ("vLLM 2026 推理引擎全解", §2.2, the kernel
+ * sketch's k_cache layout [num_pages, num_heads, page_size, head_dim]). */
+typedef struct pa_dims {
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t num_blocks;
+} pa_dims;
+
+/*
+ * pa_reshape_and_cache -- store each new token's K and V in its cache slot.
+ *
+ * Source: the step that caches K and V for reuse and appends each new token
+ * to the KV cache ("vLLM 2026 推理引擎全解", §1.1; doramagic.ai vLLM manual,
+ * "KVCacheManager 缓存管理": 追加新Token).  The slot encoding is not given by
+ * the pages; this library reads slot = physical_block * B + offset.
+ *
+ *   k, v          device, fp16 [num_tokens, H, D]: the new tokens' keys / values
+ *   k_cache       device, fp16 [N, H, B, D]: updated in place
+ *   v_cache       device, fp16 [N, H, B, D]: updated in place
+ *   slot_mapping  device, int32 [num_tokens]: slot of token i; slot < 0 skips
+ *                 the token; slot >= N * B is skipped and flags PA_DEVERR_SLOT
+ *   num_tokens    >= 0 (0 launches nothing)
+ *   dims          host; num_seqs is not used
+ *   stream        cudaStream_t
+ *
+ * For each i with 0 <= slot < N*B and every head h:
+ *   k_cache[slot / B, h, slot % B, :] = k[i, h, :]   (same for v)
+ * Copies are bit-exact.  Two tokens mapping to the same slot race.
+ */
+int pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                         const int32_t *slot_mapping, int32_t num_tokens,
+                         const pa_dims *dims, void *stream);
+
+/*
+ * pa_decode -- paged-attention decode for a batch of sequences.
+ *
+ * Source: o = Attention(q_t, K_{1:t}, V_{1:t}) ("vLLM 2026 推理引擎全解",
+ * §1.1), with K/V gathered block by block through the block table
+ * (mjmagnets.cn vLLM tutorial, §2.2; "vLLM 2026 推理引擎全解", §2.2, where the
+ * attention is computed page by page as a paged extension of FlashAttention).
+ *
+ *   out           device, fp16 [S, H, D]: written
+ *   q             device, fp16 [S, H, D]: one query per sequence and head
+ *   k_cache       device, fp16 [N, H, B, D]
+ *   v_cache       device, fp16 [N, H, B, D]
+ *   block_tables  device, int32 [S, max_blocks_per_seq]: logical -> physical
+ *                 block; only the first ceil(ctx_s / B) entries of row s are
+ *                 read, so the rest may hold anything
+ *   context_lens  device, int32 [S]: ctx_s, tokens of sequence s (0 gives a
+ *                 zero output row)
+ *   scale         softmax scale (1/sqrt(D) for standard attention)
+ *   max_blocks_per_seq  row length of block_tables (> 0)
+ *   dims, stream  as above
+ *
+ * For each s, h:  out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K_t) V_t
+ * over t < ctx_s, where K_t / V_t is row t % B of block
+ * block_tables[s, t / B] at head h.  Scores, the running max/sum softmax and
+ * the weighted sum are fp32; the output is rounded to fp16 (nearest even).
+ *
+ * Long contexts are split into partitions processed in parallel and combined
+ * on the device (by the last partition of each (sequence, head) to finish, in
+ * the same launch).  This call allocates its counter buffer and partial-result
+ * workspace itself with stream-ordered cudaMallocAsync / cudaFreeAsync (and
+ * zeroes the counters with cudaMemsetAsync); pa_decode_ws takes them from the
+ * caller instead.
+ */
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *context_lens, float scale,
+              int32_t max_blocks_per_seq, const pa_dims *dims, void *stream);
+
+/*
+ * Bytes of partial-result workspace pa_decode_ws needs for these sizes and
+ * partition length (partition_tokens = 0 selects the default).  0 means no
+ * partials are needed (every sequence fits one partition).  Returns
+ * (size_t)-1 on invalid sizes.
+ */
+size_t pa_decode_workspace_bytes(const pa_dims *dims, int32_t max_blocks_per_seq,
+                                 int32_t partition_tokens);
+
+/*
+ * Bytes of the counter buffer pa_decode_ws needs: a work-queue head, a
+ * finished-CTA count and one ticket per (sequence, head), rounded up to 256.
+ * Returns 0 on invalid sizes.
+ */
+size_t pa_decode_counters_bytes(const pa_dims *dims);
+
+/*
+ * pa_decode_ws -- pa_decode with caller-provided buffers.
+ *
+ *   partition_tokens  tokens per context partition: a positive multiple of
+ *                     block_size, or 0 for the default.  A value of at least
+ *                     max_blocks_per_seq * B processes every sequence in one
+ *                     pass with no partial results.
+ *   workspace         device, at least pa_decode_workspace_bytes(...) bytes,
+ *                     16-byte aligned; holds the partitions' partial results.
+ *                     Needs no initialisation.  May be NULL when the required
+ *                     size is 0.
+ *   workspace_bytes   its size
+ *   counters          device, at least pa_decode_counters_bytes(dims) bytes,
+ *                     4-byte aligned, ALL ZERO before the first call.  Every
+ *                     call that completes without a device error leaves it
+ *                     all zero again, so one zeroed counter buffer serves any
+ *                     number of calls of any sizes (up to its capacity).
+ *                     Calls sharing a counter buffer or a workspace must not
+ *                     overlap on the device (use one pair per stream).  After
+ *                     a device error (pa_device_errors() != 0), zero the
+ *                     counter buffer before reusing it.
+ *   counters_bytes    its size
+ */
+int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, const int32_t *context_lens, float scale,
+                 int32_t max_blocks_per_seq, const pa_dims *dims, int32_t partition_tokens,
+                 void *workspace, size_t workspace_bytes, uint32_t *counters,
+                 size_t counters_bytes, void *stream);
+
+/*
+ * Wait for `stream`, then return (in *flags, host) and clear the current
+ * device's error word: an OR of PA_DEVERR_* bits set by kernels since the last
+ * read.  The word is shared by all streams of the device.
+ */
+int pa_device_errors(void *stream, uint32_t *flags);
+
+/* Human-readable name of a pa_status value. */
+const char *pa_status_string(int status);
+
+/* cudaError_t of the most recent PA_ERR_CUDA on this host thread. */
+int pa_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

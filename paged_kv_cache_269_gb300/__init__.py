@@ -1,0 +1,282 @@
+"""PagedAttention decode on GB300: the Python binding of libpa.
+
+libpa is a C-ABI shared library of hand-written sm_103a CUDA kernels (see
+include/pa.h).  This module only marshals arguments: it checks torch tensors,
+passes their device pointers and the current CUDA stream through ctypes, and
+turns non-zero status codes into exceptions.  Every step of the computation
+runs in libpa's kernels; there is no CPU or PyTorch fallback, and a missing or
+unbuildable library raises.
+
+Functions (names follow the C ABI):
+  reshape_and_cache(k, v, k_cache, v_cache, slot_mapping)
+  decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, ...)
+  decode_workspace_bytes(...), decode_counters_bytes(...), device_errors(), version()
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+__all__ = ["PaError", "Dims", "lib", "reshape_and_cache", "decode", "decode_workspace_bytes",
+           "decode_counters_bytes", "device_errors", "reset_workspaces", "version", "DEVERR_TABLE", "DEVERR_CONTEXT",
+           "DEVERR_SLOT", "DEVERR_TIMEOUT"]
+
+DEVERR_TABLE = 0x1
+DEVERR_CONTEXT = 0x2
+DEVERR_SLOT = 0x4
+DEVERR_TIMEOUT = 0x8
+
+STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_UNSUPPORTED",
+          -4: "PA_ERR_ALIGN", -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_CUDA"}
+
+# Every symbol include/pa.h declares.
+EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_bytes",
+           "pa_decode_counters_bytes", "pa_decode_ws", "pa_device_errors", "pa_status_string",
+           "pa_last_cuda_error", "pa_version")
+_SIZE_ERROR = (1 << 64) - 1
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(l):
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    dp = ctypes.POINTER(Dims)
+    l.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, dp, vp]
+    l.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp]
+    l.pa_decode_workspace_bytes.argtypes = [dp, i32, i32]
+    l.pa_decode_workspace_bytes.restype = sz
+    l.pa_decode_counters_bytes.argtypes = [dp]
+    l.pa_decode_counters_bytes.restype = sz
+    l.pa_decode_ws.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, i32, vp, sz, vp,
+                               sz, vp]
+    l.pa_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    l.pa_status_string.argtypes = [ctypes.c_int]
+    l.pa_status_string.restype = ctypes.c_char_p
+    l.pa_last_cuda_error.argtypes = []
+    l.pa_version.argtypes = []
+    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_ws", "pa_device_errors",
+                 "pa_last_cuda_error", "pa_version"):
+        getattr(l, name).restype = ctypes.c_int
+    return l
+
+
+def lib(path: str | None = None):
+    """The loaded libpa (built first if missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.build()
+            _lib = _declare(ctypes.CDLL(p))
+        return _lib
+
+
+def version() -> int:
+    return lib().pa_version()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        l = lib()
+        msg = l.pa_status_string(rc).decode()
+        if rc == -6:
+            msg += f" (cudaError {l.pa_last_cuda_error()})"
+        raise PaError(rc, f"{what}: {STATUS.get(rc, rc)}: {msg}")
+
+
+# ----------------------------------------------------------------------------
+# torch marshalling
+# ----------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(device, stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream), stream
+
+
+def _need(t, name, dtype, ndim, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _cache_dims(k_cache, num_seqs=0):
+    N, H, B, D = k_cache.shape
+    return Dims(num_seqs, H, D, B, N)
+
+
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """k_cache[slot // B, :, slot % B, :] = k[i] (same for v) for every i with
+    slot = slot_mapping[i] >= 0.  Caches are updated in place."""
+    torch = _torch()
+    _need(k_cache, "k_cache", torch.float16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.float16, 4, dev)
+    _need(k, "k", torch.float16, 3, dev)
+    _need(v, "v", torch.float16, 3, dev)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    N, H, B, D = k_cache.shape
+    T = k.shape[0]
+    if v_cache.shape != k_cache.shape or k.shape != (T, H, D) or v.shape != k.shape \
+            or slot_mapping.shape[0] != T:
+        raise ValueError("reshape_and_cache: inconsistent shapes")
+    dims = _cache_dims(k_cache)
+    sh, _ = _stream_handle(dev, stream)
+    with torch.cuda.device(dev):
+        rc = lib().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(slot_mapping), T, ctypes.byref(dims), sh)
+    _check(rc, "pa_reshape_and_cache")
+
+
+def decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, num_blocks,
+                           max_blocks_per_seq, partition_tokens=0) -> int:
+    """Bytes of partial-result workspace pa_decode_ws needs (0: none)."""
+    dims = Dims(num_seqs, num_heads, head_dim, block_size, num_blocks)
+    n = lib().pa_decode_workspace_bytes(ctypes.byref(dims), max_blocks_per_seq, partition_tokens)
+    if n == _SIZE_ERROR:
+        raise PaError(-2, "pa_decode_workspace_bytes: invalid sizes")
+    return n
+
+
+def decode_counters_bytes(num_seqs, num_heads, head_dim=128, block_size=16, num_blocks=1) -> int:
+    """Bytes of the (zeroed, reusable) counter buffer pa_decode_ws needs."""
+    dims = Dims(num_seqs, num_heads, head_dim, block_size, num_blocks)
+    n = lib().pa_decode_counters_bytes(ctypes.byref(dims))
+    if n == 0:
+        raise PaError(-2, "pa_decode_counters_bytes: invalid sizes")
+    return n
+
+
+# Per (device, stream): a zeroed counter buffer, which every successful call
+# leaves zeroed, and a scratch workspace for partial results (no initialisation
+# needed).  Both grow on demand.
+_buffers: dict = {}
+_buf_lock = threading.Lock()
+
+
+def _buffers_for(device, stream, counters_bytes, workspace_bytes):
+    torch = _torch()
+    key = (device.index, stream.cuda_stream)
+    with _buf_lock:
+        ctr, ws = _buffers.get(key, (None, None))
+        with torch.cuda.stream(stream):
+            if ctr is None or ctr.numel() * 4 < counters_bytes:
+                ctr = torch.zeros(max(counters_bytes, 1 << 16) // 4, dtype=torch.int32,
+                                  device=device)
+            if workspace_bytes and (ws is None or ws.numel() < workspace_bytes):
+                ws = torch.empty(max(workspace_bytes, 1 << 20), dtype=torch.uint8, device=device)
+        _buffers[key] = (ctr, ws)
+        return ctr, ws
+
+
+def reset_workspaces():
+    """Zero every cached counter buffer (needed after a device error)."""
+    with _buf_lock:
+        for ctr, _ in _buffers.values():
+            ctr.zero_()
+
+
+def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+           max_blocks_per_seq=None, partition_tokens=0, workspace=None, counters=None,
+           stream=None, allocate_in_library=False):
+    """Paged-attention decode into `out` [S, H, D] fp16.
+
+    q [S, H, D] fp16; k_cache / v_cache [N, H, B, D] fp16; block_tables
+    [S, MB] int32; context_lens [S] int32.  partition_tokens = 0 picks the
+    library default.  counters (a zeroed int32 CUDA tensor of at least
+    decode_counters_bytes(...) bytes) and workspace (a uint8 CUDA tensor of at
+    least decode_workspace_bytes(...) bytes) are optional; by default cached
+    per-stream buffers are used.  allocate_in_library=True calls pa_decode,
+    which allocates both itself with cudaMallocAsync on the stream.
+    """
+    torch = _torch()
+    _need(k_cache, "k_cache", torch.float16, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", torch.float16, 4, dev)
+    _need(q, "q", torch.float16, 3, dev)
+    _need(out, "out", torch.float16, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    N, H, B, D = k_cache.shape
+    S = q.shape[0]
+    if v_cache.shape != k_cache.shape or q.shape != (S, H, D) or out.shape != q.shape \
+            or block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("decode: inconsistent shapes")
+    MB = block_tables.shape[1] if max_blocks_per_seq is None else int(max_blocks_per_seq)
+    if MB != block_tables.shape[1]:
+        raise ValueError("max_blocks_per_seq must equal block_tables.shape[1]")
+    dims = _cache_dims(k_cache, S)
+    sh, st = _stream_handle(dev, stream)
+    l = lib()
+    with torch.cuda.device(dev):
+        if allocate_in_library:
+            rc = l.pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                             _ptr(context_lens), float(scale), MB, ctypes.byref(dims), sh)
+            _check(rc, "pa_decode")
+            return out
+        need_ws = l.pa_decode_workspace_bytes(ctypes.byref(dims), MB, int(partition_tokens))
+        need_ctr = l.pa_decode_counters_bytes(ctypes.byref(dims))
+        if need_ws == _SIZE_ERROR or need_ctr == 0:
+            raise PaError(-2, "decode: invalid sizes")
+        if counters is None or (workspace is None and need_ws):
+            c2, w2 = _buffers_for(dev, st, need_ctr, need_ws)
+            counters = c2 if counters is None else counters
+            workspace = w2 if workspace is None else workspace
+        _need(counters, "counters", torch.int32, 1, dev)
+        if workspace is not None:
+            _need(workspace, "workspace", torch.uint8, 1, dev)
+        ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+        ws_n = workspace.numel() if workspace is not None else 0
+        rc = l.pa_decode_ws(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                            _ptr(context_lens), float(scale), MB, ctypes.byref(dims),
+                            int(partition_tokens), ws_ptr, ws_n, _ptr(counters),
+                            counters.numel() * 4, sh)
+    _check(rc, "pa_decode_ws")
+    return out
+
+
+def device_errors(stream=None, device=None) -> int:
+    """Synchronise the stream and return-and-clear the device error word."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    sh, _ = _stream_handle(device, stream)
+    flags = ctypes.c_uint32(0)
+    with torch.cuda.device(device):
+        rc = lib().pa_device_errors(sh, ctypes.byref(flags))
+    _check(rc, "pa_device_errors")
+    return int(flags.value)

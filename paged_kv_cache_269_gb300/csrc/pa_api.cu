@@ -1,0 +1,281 @@
+// pa_api.cu -- the C ABI of libpa (declared in include/pa.h).
+//
+// Host-side argument checking, per-device set-up, workspace sizing and the
+// launches.  Every entry point returns a pa_status; nothing here throws,
+// aborts or synchronises except pa_device_errors.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+// The device error word: kernels OR PA_DEVERR_* bits into it.
+__device__ unsigned int g_device_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultPartitionTokens = 256;
+constexpr int kVersion = 10000;  // 1.0.0
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned int *err = nullptr;  // device address of g_device_error_word
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return PA_ERR_CUDA;
+}
+
+// Set up the current device once: SM count, error-word address, kernel
+// attributes.  Returns PA_OK and the state, or PA_ERR_CUDA.
+int current_device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_cuda(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &st = g_devices[dev];
+    if (!st.ready) {
+        e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail_cuda(e);
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_device_error_word);
+        if (e != cudaSuccess) return fail_cuda(e);
+        st.err = static_cast<unsigned int *>(addr);
+        e = prepare_decode_kernels(dev);
+        if (e != cudaSuccess) return fail_cuda(e);
+        st.ready = true;
+    }
+    *out = &st;
+    return PA_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shared checks of pa_dims.  need_seqs: num_seqs is used by the call.
+int check_dims(const pa_dims *dims, bool need_seqs) {
+    if (!dims) return PA_ERR_NULL;
+    if (dims->num_heads <= 0 || dims->head_dim <= 0 || dims->block_size <= 0 ||
+        dims->num_blocks <= 0)
+        return PA_ERR_SHAPE;
+    if (need_seqs && dims->num_seqs < 0) return PA_ERR_SHAPE;
+    if (!decode_variant_supported(dims->head_dim, dims->block_size)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// Tiles per unit and number of partitions for a partition length.
+int partition_plan(const pa_dims *dims, int32_t max_blocks_per_seq, int32_t partition_tokens,
+                   int32_t *tiles_per_unit, int32_t *max_parts) {
+    if (max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+    const int B = dims->block_size;
+    if (static_cast<long long>(max_blocks_per_seq) * B > 0x7fffffffLL) return PA_ERR_SHAPE;
+    int32_t tokens = partition_tokens == 0 ? kDefaultPartitionTokens : partition_tokens;
+    if (tokens < 0 || tokens % B != 0 || tokens == 0) return PA_ERR_SHAPE;
+    int32_t tpu = tokens / B;
+    if (tpu > max_blocks_per_seq) tpu = max_blocks_per_seq;
+    *tiles_per_unit = tpu;
+    *max_parts = (max_blocks_per_seq + tpu - 1) / tpu;
+    // the work-queue index (sequence, partition, head) must fit in 32 bits
+    const long long units = static_cast<long long>(dims->num_seqs) * dims->num_heads * *max_parts;
+    if (units >= 0xffffffffLL - (1LL << 20)) return PA_ERR_SHAPE;
+    return PA_OK;
+}
+
+}  // namespace
+
+void workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t max_parts,
+                      WorkspaceLayout *out) {
+    const size_t pairs = static_cast<size_t>(num_seqs) * static_cast<size_t>(num_heads);
+    const size_t parts = max_parts > 1 ? pairs * static_cast<size_t>(max_parts) : 0;
+    WorkspaceLayout l;
+    l.counters_bytes = round_up((2 + pairs) * sizeof(uint32_t), 256);
+    l.ml_off = 0;
+    l.ml_bytes = round_up(parts * 2 * sizeof(float), 256);
+    l.acc_off = l.ml_off + l.ml_bytes;
+    l.acc_bytes = round_up(parts * static_cast<size_t>(head_dim) * sizeof(float), 256);
+    l.workspace_bytes = l.acc_off + l.acc_bytes;
+    *out = l;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                         const int32_t *slot_mapping, int32_t num_tokens, const pa_dims *dims,
+                         void *stream) {
+    int rc = check_dims(dims, false);
+    if (rc != PA_OK) return rc;
+    if (num_tokens < 0) return PA_ERR_SHAPE;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_NULL;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PA_ERR_ALIGN;
+    if (static_cast<long long>(dims->num_blocks) * dims->block_size > 0x7fffffffLL)
+        return PA_ERR_SHAPE;
+    DeviceState *st = nullptr;
+    rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    cudaError_t e = launch_reshape_and_cache(
+        static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v),
+        static_cast<uint16_t *>(k_cache), static_cast<uint16_t *>(v_cache), slot_mapping,
+        num_tokens, dims->num_heads, dims->head_dim, dims->block_size, dims->num_blocks, st->err,
+        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+size_t pa_decode_workspace_bytes(const pa_dims *dims, int32_t max_blocks_per_seq,
+                                 int32_t partition_tokens) {
+    if (check_dims(dims, true) != PA_OK) return static_cast<size_t>(-1);
+    int32_t tpu = 0, parts = 0;
+    if (partition_plan(dims, max_blocks_per_seq, partition_tokens, &tpu, &parts) != PA_OK)
+        return static_cast<size_t>(-1);
+    WorkspaceLayout l;
+    workspace_layout(dims->num_seqs, dims->num_heads, dims->head_dim, parts, &l);
+    return l.workspace_bytes;
+}
+
+size_t pa_decode_counters_bytes(const pa_dims *dims) {
+    if (check_dims(dims, true) != PA_OK) return 0;
+    WorkspaceLayout l;
+    workspace_layout(dims->num_seqs, dims->num_heads, dims->head_dim, 1, &l);
+    return l.counters_bytes;
+}
+
+int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_cache,
+                 const int32_t *block_tables, const int32_t *context_lens, float scale,
+                 int32_t max_blocks_per_seq, const pa_dims *dims, int32_t partition_tokens,
+                 void *workspace, size_t workspace_bytes, uint32_t *counters,
+                 size_t counters_bytes, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != PA_OK) return rc;
+    int32_t tpu = 0, parts = 0;
+    rc = partition_plan(dims, max_blocks_per_seq, partition_tokens, &tpu, &parts);
+    if (rc != PA_OK) return rc;
+    if (dims->num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PA_ERR_ALIGN;
+    if (!isfinite(scale)) return PA_ERR_SHAPE;
+    WorkspaceLayout l;
+    workspace_layout(dims->num_seqs, dims->num_heads, dims->head_dim, parts, &l);
+    if (!counters || counters_bytes < l.counters_bytes || !aligned(counters, 4))
+        return PA_ERR_WORKSPACE;
+    if (l.workspace_bytes > 0 &&
+        (!workspace || workspace_bytes < l.workspace_bytes || !aligned(workspace, 16)))
+        return PA_ERR_WORKSPACE;
+
+    DeviceState *st = nullptr;
+    rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    DecodeArgs a;
+    a.out = static_cast<uint16_t *>(out);
+    a.q = static_cast<const uint16_t *>(q);
+    a.k_cache = static_cast<const uint16_t *>(k_cache);
+    a.v_cache = static_cast<const uint16_t *>(v_cache);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.num_seqs = dims->num_seqs;
+    a.num_heads = dims->num_heads;
+    a.num_blocks = dims->num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.tiles_per_unit = tpu;
+    a.max_parts = parts;
+    a.counters = counters;
+    a.part_ml = parts > 1 ? reinterpret_cast<float *>(ws + l.ml_off) : nullptr;
+    a.part_acc = parts > 1 ? reinterpret_cast<float *>(ws + l.acc_off) : nullptr;
+    a.err = st->err;
+    cudaError_t e = launch_decode(a, dims->head_dim, dims->block_size, st->num_sms,
+                                  static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidConfiguration) return PA_ERR_UNSUPPORTED;  // too many sequences
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *context_lens, float scale,
+              int32_t max_blocks_per_seq, const pa_dims *dims, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != PA_OK) return rc;
+    int32_t tpu = 0, parts = 0;
+    rc = partition_plan(dims, max_blocks_per_seq, 0, &tpu, &parts);
+    if (rc != PA_OK) return rc;
+    if (dims->num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
+    WorkspaceLayout l;
+    workspace_layout(dims->num_seqs, dims->num_heads, dims->head_dim, parts, &l);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState *st = nullptr;
+    rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    // one allocation: counters first, then the partial-result workspace
+    void *buf = nullptr;
+    cudaError_t e = cudaMallocAsync(&buf, l.counters_bytes + l.workspace_bytes, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = cudaMemsetAsync(buf, 0, l.counters_bytes, s);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(buf, s);
+        return fail_cuda(e);
+    }
+    uint8_t *base = static_cast<uint8_t *>(buf);
+    rc = pa_decode_ws(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                      max_blocks_per_seq, dims, 0, l.workspace_bytes ? base + l.counters_bytes : nullptr,
+                      l.workspace_bytes, reinterpret_cast<uint32_t *>(base), l.counters_bytes,
+                      stream);
+    e = cudaFreeAsync(buf, s);
+    if (rc != PA_OK) return rc;
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+int pa_device_errors(void *stream, uint32_t *flags) {
+    if (!flags) return PA_ERR_NULL;
+    DeviceState *st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&word, st->err, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(st->err, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    *flags = word;
+    return PA_OK;
+}
+
+const char *pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_NULL: return "a required pointer is NULL";
+        case PA_ERR_SHAPE: return "invalid size";
+        case PA_ERR_UNSUPPORTED: return "unsupported head_dim, block_size or batch size";
+        case PA_ERR_ALIGN: return "fp16 pointer not 16-byte aligned";
+        case PA_ERR_WORKSPACE: return "workspace or counter buffer missing, too small or misaligned";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+int pa_last_cuda_error(void) { return t_last_cuda_error; }
+
+int pa_version(void) { return kVersion; }
+
+}  // extern "C"

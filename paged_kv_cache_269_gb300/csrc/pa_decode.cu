@@ -1,0 +1,610 @@
+// pa_decode.cu -- paged-attention decode kernel for GB300 (sm_103a).
+//
+// What it computes: for every sequence s and head h,
+//   out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K_t) V_t,  t < ctx_s,
+// where K_t / V_t is row t % B of physical block block_tables[s][t / B]
+// ("vLLM 2026 推理引擎全解：从 PagedAttention 到分离式 Prefill", §1.1 for the
+// attention, §2.1-§2.2 for the block table; mjmagnets.cn vLLM tutorial, §2.2:
+// the operator gathers the K/V blocks through the table, then computes).
+//
+// How (a GB300 design, not the pages' sketch):
+//  * Work unit = (sequence, head, partition of tiles_per_unit KV blocks).
+//    A persistent grid (CTAs per SM x SMs) pulls units from a device-wide
+//    atomic queue.  Units are ordered sequence-major, then partition, with the
+//    head fastest, so CTAs running at the same time read neighbouring 4 KiB
+//    head tiles of the same physical blocks and the same shared-prefix blocks.
+//  * Warp specialisation.  One producer warp reads each unit's block-table
+//    slice with one coalesced load and streams whole K and V tiles (B x D
+//    fp16, contiguous in the [N, H, B, D] layout) into a ring of shared-memory
+//    stages with the bulk asynchronous copy engine (cp.async.bulk, completion
+//    on an mbarrier).  NC consumer warps take the unit's tiles round-robin.
+//  * Per tile, a consumer warp computes the q.k scores with 16-byte shared
+//    loads and xor-shuffle reductions, updates a running max / sum softmax in
+//    fp32 (the FlashAttention-style page-by-page computation the pages
+//    describe, "vLLM 2026 推理引擎全解", §2.2), and accumulates p * V in fp32.
+//  * At the end of a unit the NC warps' (max, sum, acc) states are merged in
+//    shared memory by one warp.  A unit covering the whole context writes the
+//    fp16 output directly.  Otherwise it writes its partial to the workspace
+//    and takes a ticket; the last partition of a (sequence, head) to finish
+//    combines all partials and writes the output (split-context reduce in the
+//    same launch, no second kernel).
+//  * No tensor cores: single-query decode is a bandwidth-bound GEMV.
+#include <cuda_fp16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+constexpr int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+template <int D, int B>
+struct Cfg {
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+    static_assert(B == 8 || B == 16 || B == 32, "block_size");
+    static constexpr int NC = 8;                      // consumer warps
+    static constexpr int THREADS = (NC + 1) * 32;     // + one producer warp
+    static constexpr int TILE_BYTES = B * D * 2;      // one K (or V) tile, fp16
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int STAGE_BUDGET = 80 * 1024;
+    static constexpr int NS = clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, 16);
+    static constexpr int ND = 4;                      // unit descriptor slots
+    // q.k layout: LPT lanes per token, 8 dims (16 bytes) per lane.
+    static constexpr int LPT = D / 8;
+    static constexpr int TPR = 32 / LPT;              // tokens per row group
+    static constexpr int RG = B / TPR;                // row groups per tile
+    static_assert(RG * TPR == B, "tile rows");
+    // p.V layout: DPL dims per lane.
+    static constexpr int DPL = D / 32;
+
+    static constexpr int OFF_STAGES = 0;
+    static constexpr int OFF_DESC_Q = NS * STAGE_BYTES;
+    static constexpr int OFF_MERGE_ACC = OFF_DESC_Q + ND * D * 2;
+    static constexpr int OFF_MERGE_ML = OFF_MERGE_ACC + ND * NC * D * 4;
+    static constexpr int OFF_PROBS = OFF_MERGE_ML + ND * NC * 8;
+    static constexpr int OFF_META = OFF_PROBS + NC * B * 4;
+    static constexpr int META_INTS = 8;
+    static constexpr int OFF_STAGE_OK = OFF_META + ND * META_INTS * 4;
+    static constexpr int OFF_STAGE_TAG = OFF_STAGE_OK + NS * 4;
+    static constexpr int OFF_BARS = (OFF_STAGE_TAG + NS * 4 + 7) / 8 * 8;
+    static constexpr int NUM_BARS = 2 * NS + 3 * ND;
+    static constexpr int OFF_FLAGS = OFF_BARS + NUM_BARS * 8;
+    static constexpr int OFF_SEQ = OFF_FLAGS + 16;    // prefix[S + 1], ctx[S]
+
+    // Two CTAs per SM when the shared-memory footprint allows it.
+    static constexpr int MIN_BLOCKS = (OFF_SEQ + 4096 <= 110 * 1024) ? 2 : 1;
+
+    static size_t smem_bytes(int num_seqs) {
+        return static_cast<size_t>(OFF_SEQ) + (2 * static_cast<size_t>(num_seqs) + 1) * 4;
+    }
+};
+
+__device__ __forceinline__ float2 h2f(uint32_t bits) {
+    __half2 h = *reinterpret_cast<const __half2 *>(&bits);
+    return __half22float2(h);
+}
+
+// One KV tile of one unit, processed by one warp.
+template <int D, int B>
+__device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t *vtile,
+                                             const float (&qf)[8], float scale_log2, int nvalid,
+                                             float &run_max, float &run_sum,
+                                             float (&acc)[Cfg<D, B>::DPL], float *probs,
+                                             int lane) {
+    using C = Cfg<D, B>;
+    const int c = lane % C::LPT;   // 16-byte column of the row
+    const int tr = lane / C::LPT;  // token within the row group
+
+    // scores: partial dot products over this lane's 8 dims
+    float sc[C::RG];
+    const uint4 *K4 = reinterpret_cast<const uint4 *>(ktile);
+#pragma unroll
+    for (int r = 0; r < C::RG; ++r) {
+        const uint4 kv = K4[(r * C::TPR + tr) * C::LPT + c];
+        const float2 k0 = h2f(kv.x), k1 = h2f(kv.y), k2 = h2f(kv.z), k3 = h2f(kv.w);
+        float dot = qf[0] * k0.x;
+        dot = fmaf(qf[1], k0.y, dot);
+        dot = fmaf(qf[2], k1.x, dot);
+        dot = fmaf(qf[3], k1.y, dot);
+        dot = fmaf(qf[4], k2.x, dot);
+        dot = fmaf(qf[5], k2.y, dot);
+        dot = fmaf(qf[6], k3.x, dot);
+        dot = fmaf(qf[7], k3.y, dot);
+        sc[r] = dot;
+    }
+#pragma unroll
+    for (int r = 0; r < C::RG; ++r) {
+#pragma unroll
+        for (int off = C::LPT / 2; off >= 1; off >>= 1)
+            sc[r] += __shfl_xor_sync(kFull, sc[r], off);
+    }
+
+    // scale into the log2 domain, mask the tokens past the context, tile max
+    float tile_max = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < C::RG; ++r) {
+        const int t = r * C::TPR + tr;
+        sc[r] = (t < nvalid) ? sc[r] * scale_log2 : -INFINITY;
+        tile_max = fmaxf(tile_max, sc[r]);
+    }
+#pragma unroll
+    for (int off = C::LPT; off < 32; off <<= 1)
+        tile_max = fmaxf(tile_max, __shfl_xor_sync(kFull, tile_max, off));
+
+    // online softmax update
+    const float new_max = fmaxf(run_max, tile_max);
+    const float alpha = exp2f(run_max - new_max);
+    float psum = 0.f;
+#pragma unroll
+    for (int r = 0; r < C::RG; ++r) {
+        sc[r] = exp2f(sc[r] - new_max);
+        psum += sc[r];
+    }
+#pragma unroll
+    for (int off = C::LPT; off < 32; off <<= 1) psum += __shfl_xor_sync(kFull, psum, off);
+    run_sum = run_sum * alpha + psum;
+    run_max = new_max;
+#pragma unroll
+    for (int i = 0; i < C::DPL; ++i) acc[i] *= alpha;
+
+    // publish the B probabilities to the whole warp
+    if (c == 0) {
+#pragma unroll
+        for (int r = 0; r < C::RG; ++r) probs[r * C::TPR + tr] = sc[r];
+    }
+    __syncwarp();
+
+    // p.V: this lane owns dims [lane * DPL, lane * DPL + DPL)
+    const uint8_t *vrow = vtile + lane * C::DPL * 2;
+    auto accumulate_row = [&](int t) {
+        const float p = probs[t];
+        const uint8_t *src = vrow + t * D * 2;
+        if constexpr (C::DPL == 2) {
+            const float2 v = h2f(*reinterpret_cast<const uint32_t *>(src));
+            acc[0] = fmaf(p, v.x, acc[0]);
+            acc[1] = fmaf(p, v.y, acc[1]);
+        } else if constexpr (C::DPL == 4) {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(src);
+            const float2 v0 = h2f(raw.x), v1 = h2f(raw.y);
+            acc[0] = fmaf(p, v0.x, acc[0]);
+            acc[1] = fmaf(p, v0.y, acc[1]);
+            acc[2] = fmaf(p, v1.x, acc[2]);
+            acc[3] = fmaf(p, v1.y, acc[3]);
+        } else {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+            const float2 v0 = h2f(raw.x), v1 = h2f(raw.y), v2 = h2f(raw.z), v3 = h2f(raw.w);
+            acc[0] = fmaf(p, v0.x, acc[0]);
+            acc[1] = fmaf(p, v0.y, acc[1]);
+            acc[2] = fmaf(p, v1.x, acc[2]);
+            acc[3] = fmaf(p, v1.y, acc[3]);
+            acc[4] = fmaf(p, v2.x, acc[4]);
+            acc[5] = fmaf(p, v2.y, acc[5]);
+            acc[6] = fmaf(p, v3.x, acc[6]);
+            acc[7] = fmaf(p, v3.y, acc[7]);
+        }
+    };
+    if (nvalid == B) {
+#pragma unroll
+        for (int t = 0; t < B; ++t) accumulate_row(t);
+    } else {
+        // rows past the context may hold anything (even NaN): skip, never
+        // multiply them by a zero weight
+#pragma unroll
+        for (int t = 0; t < B; ++t)
+            if (t < nvalid) accumulate_row(t);
+    }
+    __syncwarp();  // probs is rewritten by the next tile
+}
+
+template <int DPL>
+__device__ __forceinline__ void store_out_f16(uint16_t *dst, const float (&v)[DPL], float inv) {
+    __half h[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) h[i] = __float2half_rn(v[i] * inv);
+    if constexpr (DPL == 2) {
+        *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(h);
+    } else if constexpr (DPL == 4) {
+        *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(h);
+    } else {
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(h);
+    }
+}
+
+template <int DPL>
+__device__ __forceinline__ void load_f32(const float *src, float (&v)[DPL], bool bypass_l1) {
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2) {
+        const float2 x = bypass_l1 ? __ldcg(reinterpret_cast<const float2 *>(src + i))
+                                   : *reinterpret_cast<const float2 *>(src + i);
+        v[i] = x.x;
+        v[i + 1] = x.y;
+    }
+}
+
+template <int DPL>
+__device__ __forceinline__ void store_f32(float *dst, const float (&v)[DPL]) {
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2)
+        *reinterpret_cast<float2 *>(dst + i) = make_float2(v[i], v[i + 1]);
+}
+
+template <int D, int B>
+__global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
+    decode_kernel(const DecodeArgs a) {
+    using C = Cfg<D, B>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BARS);
+    uint64_t *empty = full + C::NS;
+    uint64_t *desc_full = empty + C::NS;
+    uint64_t *desc_empty = desc_full + C::ND;
+    uint64_t *merge_full = desc_empty + C::ND;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);
+    int *meta = reinterpret_cast<int *>(smem + C::OFF_META);
+    int *stage_ok = reinterpret_cast<int *>(smem + C::OFF_STAGE_OK);
+    // stage_tag[st] = index of the last tile the producer issued into stage st.
+    // Different consumer warps use successive fills of one stage, so a warp may
+    // reach a stage before the previous fill has landed; waiting for the tag
+    // first guarantees that the fill before the awaited one has completed,
+    // which keeps the mbarrier parity wait unambiguous.
+    volatile uint32_t *stage_tag = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_STAGE_TAG);
+    float *merge_acc = reinterpret_cast<float *>(smem + C::OFF_MERGE_ACC);
+    float2 *merge_ml = reinterpret_cast<float2 *>(smem + C::OFF_MERGE_ML);
+    uint16_t *desc_q = reinterpret_cast<uint16_t *>(smem + C::OFF_DESC_Q);
+    const int S = a.num_seqs;
+    const int H = a.num_heads;
+    int *prefix = reinterpret_cast<int *>(smem + C::OFF_SEQ);  // [S + 1]
+    int *ctx_of = prefix + S + 1;                              // [S]
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int TPU = a.tiles_per_unit;
+
+    // ---- prologue: barriers, per-sequence context lengths and unit counts
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+            stage_tag[i] = 0xffffffffu;
+        }
+        for (int i = 0; i < C::ND; ++i) {
+            mbar_init(&desc_full[i], 1);
+            mbar_init(&desc_empty[i], C::NC);
+            mbar_init(&merge_full[i], C::NC);
+        }
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    const int ctx_cap = a.max_blocks_per_seq * B;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+        int c = a.context_lens[s];
+        if (c < 0 || c > ctx_cap) {
+            atomicOr(a.err, PA_DEVERR_CONTEXT);
+            c = c < 0 ? 0 : ctx_cap;
+        }
+        const int nblk = (c + B - 1) / B;
+        ctx_of[s] = c;
+        prefix[s + 1] = nblk == 0 ? 1 : (nblk + TPU - 1) / TPU;  // partitions of s
+    }
+    __syncthreads();
+    if (warp == C::NC) {  // exclusive prefix over sequences of their partition counts
+        int running = 0;
+        for (int base = 0; base < S; base += 32) {
+            const int s = base + lane;
+            int v = s < S ? prefix[s + 1] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(kFull, v, off);
+                if (lane >= off) v += y;
+            }
+            if (s < S) prefix[s + 1] = running + v;
+            running += __shfl_sync(kFull, v, 31);
+        }
+        if (lane == 0) prefix[0] = 0;
+    }
+    __syncthreads();
+
+    const uint32_t num_units = static_cast<uint32_t>(prefix[S]) * static_cast<uint32_t>(H);
+
+    if (warp == C::NC) {
+        // ================= producer warp =================
+        uint32_t kq = 0;  // tiles issued
+        uint32_t dq = 0;  // unit descriptors issued
+        bool ok = true;
+        uint32_t pending = 0;
+        if (lane == 0) pending = atomicAdd(&a.counters[0], 1u);
+        while (true) {
+            const uint32_t u = __shfl_sync(kFull, pending, 0);
+            if (u >= num_units) break;
+            if (lane == 0) pending = atomicAdd(&a.counters[0], 1u);  // prefetch the next grab
+            const int g = static_cast<int>(u / H);
+            const int h = static_cast<int>(u - static_cast<uint32_t>(g) * H);
+            int lo = 0, hi = S - 1;  // sequence s with prefix[s] <= g < prefix[s + 1]
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
+            }
+            const int s = lo;
+            const int p = g - prefix[s];
+            const int np = prefix[s + 1] - prefix[s];
+            const int ctx = ctx_of[s];
+            const int nblk = (ctx + B - 1) / B;
+            const int t0 = p * TPU;
+            const int nt = max(0, min(TPU, nblk - t0));
+
+            const int slot = static_cast<int>(dq % C::ND);
+            bool w_ok = mbar_wait(&desc_empty[slot], ((dq / C::ND) & 1u) ^ 1u, abort_flag, a.err);
+            if (!__all_sync(kFull, w_ok)) { ok = false; break; }
+            if (lane == 0) {
+                int *m = meta + slot * C::META_INTS;
+                m[0] = s; m[1] = h; m[2] = p; m[3] = nt; m[4] = ctx; m[5] = np;
+                mbar_arrive_expect_tx(&desc_full[slot], D * 2);
+                bulk_copy_g2s(desc_q + slot * D, a.q + (static_cast<size_t>(s) * H + h) * D, D * 2,
+                              &desc_full[slot]);
+            }
+            ++dq;
+
+            const int32_t *row = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + t0;
+            for (int j0 = 0; j0 < nt && ok; j0 += 32) {
+                const int n = min(32, nt - j0);
+                const int phys_lane = lane < n ? __ldg(row + j0 + lane) : 0;
+                for (int jj = 0; jj < n; ++jj) {
+                    const int phys = __shfl_sync(kFull, phys_lane, jj);
+                    const int st = static_cast<int>(kq % C::NS);
+                    w_ok = mbar_wait(&empty[st], ((kq / C::NS) & 1u) ^ 1u, abort_flag, a.err);
+                    if (!__all_sync(kFull, w_ok)) { ok = false; break; }
+                    if (lane == 0) {
+                        const bool in_pool = static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks);
+                        stage_ok[st] = in_pool ? 1 : 0;
+                        stage_tag[st] = kq;
+                        if (in_pool) {
+                            const size_t off = (static_cast<size_t>(phys) * H + h) * (B * D);
+                            uint8_t *dst = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
+                            mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES);
+                            bulk_copy_g2s(dst, a.k_cache + off, C::TILE_BYTES, &full[st]);
+                            bulk_copy_g2s(dst + C::TILE_BYTES, a.v_cache + off, C::TILE_BYTES, &full[st]);
+                        } else {
+                            atomicOr(a.err, PA_DEVERR_TABLE);
+                            mbar_arrive(&full[st]);
+                        }
+                    }
+                    ++kq;
+                }
+            }
+            if (!ok) break;
+        }
+        if (ok) {  // tell the consumers there is no more work
+            const int slot = static_cast<int>(dq % C::ND);
+            const bool w_ok = mbar_wait(&desc_empty[slot], ((dq / C::ND) & 1u) ^ 1u, abort_flag, a.err);
+            if (__all_sync(kFull, w_ok)) {
+                if (lane == 0) {
+                    meta[slot * C::META_INTS] = -1;
+                    mbar_arrive(&desc_full[slot]);
+                }
+                ++dq;
+            } else {
+                ok = false;
+            }
+        }
+        if (lane == 0) {
+            if (ok) {
+                // The last CTA to finish resets the work queue for the next call.
+                __threadfence();
+                const uint32_t done = atomicAdd(&a.counters[1], 1u);
+                if (done == gridDim.x - 1) {
+                    __threadfence();
+                    atomicExch(&a.counters[0], 0u);
+                    atomicExch(&a.counters[1], 0u);
+                }
+            } else {
+                // Let every copy already issued land before the CTA exits.
+                for (uint32_t k = kq > C::NS ? kq - C::NS : 0; k < kq; ++k)
+                    mbar_wait_drain(&full[k % C::NS], (k / C::NS) & 1u);
+                for (uint32_t d = dq > C::ND ? dq - C::ND : 0; d < dq; ++d)
+                    mbar_wait_drain(&desc_full[d % C::ND], (d / C::ND) & 1u);
+            }
+        }
+        return;
+    }
+
+    // ================= consumer warps =================
+    const int w = warp;
+    float *probs = reinterpret_cast<float *>(smem + C::OFF_PROBS) + w * B;
+    uint32_t kq = 0, dq = 0;
+    while (true) {
+        const int slot = static_cast<int>(dq % C::ND);
+        bool w_ok = mbar_wait(&desc_full[slot], (dq / C::ND) & 1u, abort_flag, a.err);
+        if (!__all_sync(kFull, w_ok)) return;
+        const int *m = meta + slot * C::META_INTS;
+        const int s = m[0];
+        if (s < 0) break;
+        const int h = m[1], p = m[2], nt = m[3], ctx = m[4], np = m[5];
+
+        float qf[8];
+        {
+            const uint4 qraw =
+                *reinterpret_cast<const uint4 *>(desc_q + slot * D + (lane % C::LPT) * 8);
+            const float2 q0 = h2f(qraw.x), q1 = h2f(qraw.y), q2 = h2f(qraw.z), q3 = h2f(qraw.w);
+            qf[0] = q0.x; qf[1] = q0.y; qf[2] = q1.x; qf[3] = q1.y;
+            qf[4] = q2.x; qf[5] = q2.y; qf[6] = q3.x; qf[7] = q3.y;
+        }
+        float run_max = -INFINITY, run_sum = 0.f;
+        float acc[C::DPL];
+#pragma unroll
+        for (int i = 0; i < C::DPL; ++i) acc[i] = 0.f;
+
+        for (int j = w; j < nt; j += C::NC) {
+            const uint32_t k = kq + j;
+            const int st = static_cast<int>(k % C::NS);
+            w_ok = wait_value(&stage_tag[st], k, abort_flag, a.err) &&
+                   mbar_wait(&full[st], (k / C::NS) & 1u, abort_flag, a.err);
+            if (!__all_sync(kFull, w_ok)) return;
+            if (stage_ok[st]) {
+                const int tok0 = (p * TPU + j) * B;
+                const int nvalid = min(B, ctx - tok0);
+                const uint8_t *ktile = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
+                consume_tile<D, B>(ktile, ktile + C::TILE_BYTES, qf, a.scale_log2, nvalid, run_max,
+                                   run_sum, acc, probs, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        kq += nt;
+
+        // hand this warp's state to the unit's owner warp
+        store_f32<C::DPL>(merge_acc + (slot * C::NC + w) * D + lane * C::DPL, acc);
+        if (lane == 0) merge_ml[slot * C::NC + w] = make_float2(run_max, run_sum);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&merge_full[slot]);
+
+        const int owner = static_cast<int>(dq % C::NC);
+        if (w == owner) {
+            w_ok = mbar_wait(&merge_full[slot], (dq / C::ND) & 1u, abort_flag, a.err);
+            if (!__all_sync(kFull, w_ok)) return;
+            float M = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < C::NC; ++i) M = fmaxf(M, merge_ml[slot * C::NC + i].x);
+            float L = 0.f;
+            float o[C::DPL];
+#pragma unroll
+            for (int i = 0; i < C::DPL; ++i) o[i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < C::NC; ++i) {
+                const float2 ml = merge_ml[slot * C::NC + i];
+                if (ml.x == -INFINITY) continue;  // a warp with no tile of this unit
+                const float f = exp2f(ml.x - M);
+                L = fmaf(f, ml.y, L);
+                float v[C::DPL];
+                load_f32<C::DPL>(merge_acc + (slot * C::NC + i) * D + lane * C::DPL, v, false);
+#pragma unroll
+                for (int e = 0; e < C::DPL; ++e) o[e] = fmaf(f, v[e], o[e]);
+            }
+            const size_t sh = static_cast<size_t>(s) * H + h;
+            if (np == 1) {
+                store_out_f16<C::DPL>(a.out + sh * D + lane * C::DPL, o, L > 0.f ? 1.f / L : 0.f);
+            } else {
+                const size_t pidx = sh * a.max_parts + p;
+                if (lane == 0) reinterpret_cast<float2 *>(a.part_ml)[pidx] = make_float2(M, L);
+                store_f32<C::DPL>(a.part_acc + pidx * D + lane * C::DPL, o);
+                __threadfence();
+                __syncwarp();
+                uint32_t ticket = 0;
+                if (lane == 0) ticket = atomicAdd(&a.counters[2 + sh], 1u);
+                ticket = __shfl_sync(kFull, ticket, 0);
+                if (ticket == static_cast<uint32_t>(np - 1)) {
+                    // last partition of (s, h): combine all partials
+                    __threadfence();
+                    const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml) + sh * a.max_parts;
+                    const float *pacc = a.part_acc + sh * a.max_parts * D + lane * C::DPL;
+                    float GM = -INFINITY;
+                    for (int i = lane; i < np; i += 32) GM = fmaxf(GM, __ldcg(pml + i).x);
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        GM = fmaxf(GM, __shfl_xor_sync(kFull, GM, off));
+                    float GL = 0.f;
+                    float go[C::DPL];
+#pragma unroll
+                    for (int e = 0; e < C::DPL; ++e) go[e] = 0.f;
+#pragma unroll 4
+                    for (int i = 0; i < np; ++i) {
+                        const float2 ml = __ldcg(pml + i);
+                        float v[C::DPL];
+                        load_f32<C::DPL>(pacc + static_cast<size_t>(i) * D, v, true);
+                        const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - GM);
+                        GL = fmaf(f, ml.y, GL);
+#pragma unroll
+                        for (int e = 0; e < C::DPL; ++e) go[e] = fmaf(f, v[e], go[e]);
+                    }
+                    store_out_f16<C::DPL>(a.out + sh * D + lane * C::DPL, go,
+                                          GL > 0.f ? 1.f / GL : 0.f);
+                    if (lane == 0) atomicExch(&a.counters[2 + sh], 0u);  // ready for the next call
+                }
+            }
+            __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(&desc_empty[slot]);
+        ++dq;
+    }
+}
+
+struct Variant {
+    int head_dim, block_size;
+    const void *kernel;
+    int threads;
+    size_t (*smem_bytes)(int);
+};
+
+template <int D, int B>
+Variant make_variant() {
+    return Variant{D, B, reinterpret_cast<const void *>(&decode_kernel<D, B>), Cfg<D, B>::THREADS,
+                   &Cfg<D, B>::smem_bytes};
+}
+
+const Variant *find_variant(int head_dim, int block_size) {
+    static const Variant variants[] = {
+        make_variant<64, 8>(),  make_variant<64, 16>(),  make_variant<64, 32>(),
+        make_variant<128, 8>(), make_variant<128, 16>(), make_variant<128, 32>(),
+        make_variant<256, 8>(), make_variant<256, 16>(), make_variant<256, 32>(),
+    };
+    for (const Variant &v : variants)
+        if (v.head_dim == head_dim && v.block_size == block_size) return &v;
+    return nullptr;
+}
+
+// Largest dynamic shared memory a CTA may opt into, per device (set by
+// prepare_decode_kernels before any launch on that device).
+constexpr int kMaxDevices = 64;
+int g_max_dynamic_smem[kMaxDevices] = {0};
+
+}  // namespace
+
+bool decode_variant_supported(int head_dim, int block_size) {
+    return find_variant(head_dim, block_size) != nullptr;
+}
+
+cudaError_t prepare_decode_kernels(int device) {
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess) return e;
+    static const int dims[] = {64, 128, 256};
+    static const int blocks[] = {8, 16, 32};
+    for (int d : dims)
+        for (int b : blocks) {
+            const Variant *v = find_variant(d, b);
+            e = cudaFuncSetAttribute(v->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            if (e != cudaSuccess) return e;
+        }
+    g_max_dynamic_smem[device] = optin;
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeArgs &args, int head_dim, int block_size, int num_sms,
+                          cudaStream_t stream) {
+    const Variant *v = find_variant(head_dim, block_size);
+    if (!v) return cudaErrorInvalidValue;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    const size_t smem = v->smem_bytes(args.num_seqs);
+    if (smem > static_cast<size_t>(g_max_dynamic_smem[device])) return cudaErrorInvalidConfiguration;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v->kernel, v->threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    // Persistent grid; never more CTAs than the most work units there can be.
+    const long long max_units = static_cast<long long>(args.num_seqs) * args.num_heads * args.max_parts;
+    long long grid = static_cast<long long>(per_sm) * num_sms;
+    if (grid > max_units) grid = max_units;
+    if (grid < 1) grid = 1;
+    void *params[] = {const_cast<DecodeArgs *>(&args)};
+    return cudaLaunchKernel(v->kernel, dim3(static_cast<unsigned>(grid)), dim3(v->threads), params,
+                            smem, stream);
+}
+
+}  // namespace pa

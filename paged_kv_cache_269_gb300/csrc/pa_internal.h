@@ -1,0 +1,61 @@
+// pa_internal.h -- declarations shared by the translation units of libpa.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Arguments of one decode launch (device pointers unless noted).
+struct DecodeArgs {
+    uint16_t *out;                 // fp16 [S, H, D]
+    const uint16_t *q;             // fp16 [S, H, D]
+    const uint16_t *k_cache;       // fp16 [N, H, B, D]
+    const uint16_t *v_cache;       // fp16 [N, H, B, D]
+    const int32_t *block_tables;   // [S, max_blocks_per_seq]
+    const int32_t *context_lens;   // [S]
+    float scale_log2;              // softmax scale * log2(e)
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t num_blocks;
+    int32_t max_blocks_per_seq;
+    int32_t tiles_per_unit;        // KV blocks per partition (work unit)
+    int32_t max_parts;             // ceil(max_blocks_per_seq / tiles_per_unit)
+    float *part_ml;                // [S * H * max_parts * 2]: (running max, sum) per partition
+    float *part_acc;               // [S * H * max_parts * D]: unnormalised partial outputs
+    uint32_t *counters;            // [2 + S * H]: work queue, finished CTAs, per-(s,h) tickets
+    unsigned int *err;             // device error word
+};
+
+// Sizes of the two caller buffers of pa_decode_ws.
+//   counters: [2 + S * H] uint32 (queue head, finished CTAs, per-(s,h) tickets)
+//   workspace: partial (max, sum) pairs [S * H * max_parts * 2] floats, then
+//              partial outputs [S * H * max_parts * D] floats; empty when
+//              max_parts == 1.
+struct WorkspaceLayout {
+    size_t counters_bytes;
+    size_t ml_off, ml_bytes;
+    size_t acc_off, acc_bytes;
+    size_t workspace_bytes;
+};
+
+void workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t max_parts,
+                      WorkspaceLayout *out);
+
+// Kernel launchers (pa_decode.cu / pa_cache.cu).  They return a cudaError_t.
+// `num_sms` sizes the persistent decode grid.
+cudaError_t launch_decode(const DecodeArgs &args, int head_dim, int block_size, int num_sms,
+                          cudaStream_t stream);
+bool decode_variant_supported(int head_dim, int block_size);
+cudaError_t prepare_decode_kernels(int device);
+
+cudaError_t launch_reshape_and_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,
+                                     uint16_t *v_cache, const int32_t *slot_mapping,
+                                     int32_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                     int32_t block_size, int32_t num_blocks, unsigned int *err,
+                                     cudaStream_t stream);
+
+}  // namespace pa

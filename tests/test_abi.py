@@ -1,0 +1,108 @@
+"""The C ABI library: it loads, exports every declared symbol, and rejects bad
+arguments on the host (no CUDA call is reached, so this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_269_gb300 as pa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return pa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(pa.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.pa_version() >= 10000
+    for code in pa.STATUS:
+        assert lib.pa_status_string(code)
+    assert lib.pa_status_string(12345) == b"unknown status"
+
+
+def _dims(S=2, H=4, D=128, B=16, N=32):
+    return pa.Dims(S, H, D, B, N)
+
+
+SIZE_ERROR = (1 << 64) - 1
+
+
+def test_workspace_bytes(lib):
+    d = _dims(S=64, H=32, D=128, B=16, N=5000)
+    single = lib.pa_decode_workspace_bytes(ctypes.byref(d), 128, 128 * 16)
+    split = lib.pa_decode_workspace_bytes(ctypes.byref(d), 128, 256)
+    assert single == 0 < split
+    # 8 partitions x 64 x 32 pairs x (128 acc + 2) floats
+    assert split >= 64 * 32 * 8 * 130 * 4
+    assert lib.pa_decode_workspace_bytes(ctypes.byref(d), 128, 17) == SIZE_ERROR  # not k*B
+    assert lib.pa_decode_workspace_bytes(ctypes.byref(d), 0, 256) == SIZE_ERROR
+    assert lib.pa_decode_workspace_bytes(None, 128, 256) == SIZE_ERROR
+    ctr = lib.pa_decode_counters_bytes(ctypes.byref(d))
+    assert ctr >= (2 + 64 * 32) * 4 and ctr % 256 == 0
+    assert lib.pa_decode_counters_bytes(None) == 0
+
+
+@pytest.mark.parametrize("D,B,expect", [(96, 16, -3), (128, 12, -3), (0, 16, -2), (128, 0, -2)])
+def test_decode_rejects_dims(lib, D, B, expect):
+    d = _dims(D=D, B=B)
+    rc = lib.pa_decode_ws(None, None, None, None, None, None, 0.1, 8, ctypes.byref(d), 0,
+                          None, 0, None, 0, None)
+    assert rc == expect
+
+
+def test_decode_rejects_null_and_alignment(lib):
+    d = _dims()
+    fake = ctypes.c_void_p(0x100000)           # never dereferenced: checks fail first
+    big = 1 << 20
+
+    def call(out=fake, ws=fake, ws_n=big, ctr=fake, ctr_n=big, scale=0.1, mb=8, P=0):
+        return lib.pa_decode_ws(out, fake, fake, fake, fake, fake, scale, mb, ctypes.byref(d), P,
+                                ws, ws_n, ctr, ctr_n, None)
+
+    assert call(out=None) == -1
+    assert call(out=ctypes.c_void_p(0x100002)) == -4
+    assert call(ctr=None) == -5
+    assert call(ctr_n=16) == -5                  # counter buffer too small
+    assert call(ws=None, P=16) == -5             # partials needed but no workspace
+    assert call(ws_n=16, P=16) == -5
+    assert call(scale=float("nan")) == -2
+    assert call(mb=0) == -2
+    assert call(P=24) == -2                      # not a multiple of block_size
+    assert lib.pa_decode(fake, fake, fake, fake, fake, fake, 0.1, 0, ctypes.byref(d), None) == -2
+    assert lib.pa_decode(fake, fake, fake, fake, fake, fake, 0.1, 8, None, None) == -1
+
+
+def test_empty_batches_are_noops(lib):
+    d = _dims(S=0)
+    assert lib.pa_decode_ws(None, None, None, None, None, None, 0.1, 8, ctypes.byref(d), 0,
+                            None, 0, None, 0, None) == 0
+    assert lib.pa_reshape_and_cache(None, None, None, None, None, 0, ctypes.byref(d), None) == 0
+
+
+def test_reshape_rejects(lib):
+    d = _dims()
+    fake = ctypes.c_void_p(0x100000)
+    assert lib.pa_reshape_and_cache(fake, fake, fake, fake, fake, -1, ctypes.byref(d), None) == -2
+    assert lib.pa_reshape_and_cache(fake, None, fake, fake, fake, 4, ctypes.byref(d), None) == -1
+    odd = ctypes.c_void_p(0x100008)
+    assert lib.pa_reshape_and_cache(fake, odd, fake, fake, fake, 4, ctypes.byref(d), None) == -4
+    bad = _dims(D=80)
+    assert lib.pa_reshape_and_cache(fake, fake, fake, fake, fake, 4, ctypes.byref(bad), None) == -3

@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every test here runs libpa's sm_103a kernels on cuda:0 and compares element by
+element with the oracle on the same seeded inputs.  reshape_and_cache must be
+bit-exact; decode must meet the tolerance in gpu_helpers.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import assert_parity, run_gpu, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_269_gb300 as pa
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    pa.lib()
+    pa.device_errors()  # start from a clear error word
+    return d
+
+
+def _ragged(name, lens, H=4, D=128, B=16, seed=7, **kw):
+    return workloads.build_case(name, lens, num_heads=H, head_dim=D, block_size=B, seed=seed,
+                                **kw)
+
+
+# ----------------------------------------------------------------------------
+# small cases: several tiles, ragged tails, every partition regime
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("partition_tokens", [0, 16, 32, 48, 256, 4096])
+def test_tiny_workload(dev, partition_tokens):
+    case = workloads.make_workload("tiny", new_tokens=True)
+    got, flags, _ = run_gpu(case, dev, partition_tokens)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), f"tiny P={partition_tokens}")
+
+
+EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 255, 256, 257, 511, 512, 513, 1000, 4096]
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 16, 240, 272, 1 << 16])
+def test_edge_lengths(dev, partition_tokens):
+    case = _ragged("edges", EDGE_LENS, H=3)
+    got, flags, _ = run_gpu(case, dev, partition_tokens)
+    assert flags == 0
+    ref = oracle.decode_case(case)
+    assert_parity(got, ref, f"edges P={partition_tokens}")
+    assert (got[0] == 0).all(), "an empty context must give a zero row"
+    # a one-token context returns that token's V row exactly (weight 1.0)
+    phys = case.block_tables[1, 0]
+    assert np.array_equal(got[1].view(np.uint16), case.v_cache[phys, :, 0, :].view(np.uint16))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_head_dim_block_size_variants(dev, D, B):
+    case = _ragged(f"v{D}_{B}", [1, 7, B - 1, B, B + 1, 100, 333, 700], H=2, D=D, B=B,
+                   seed=D + B)
+    ref = oracle.decode_case(case)
+    for P in (0, 2 * B, 5 * B):
+        got, flags, _ = run_gpu(case, dev, P)
+        assert flags == 0
+        assert_parity(got, ref, f"D={D} B={B} P={P}")
+
+
+def test_split_matches_single_pass(dev):
+    rng = np.random.default_rng(17)
+    case = _ragged("split", rng.integers(1, 3000, size=24), H=8)
+    ref = oracle.decode_case(case)
+    single, f1, d = run_gpu(case, dev, 1 << 20)
+    split, f2, _ = run_gpu(case, dev, 128, tensors=d)
+    assert f1 == 0 and f2 == 0
+    assert_parity(single, ref, "single pass")
+    assert_parity(split, ref, "split")
+    assert_parity(split, single.astype(np.float64), "split vs single pass")
+
+
+def test_deterministic_and_stream(dev):
+    import torch
+    case = workloads.make_workload("tiny")
+    a, _, d = run_gpu(case, dev, 32)
+    b, _, _ = run_gpu(case, dev, 32, tensors=d)
+    s = torch.cuda.Stream(dev)
+    c, flags, _ = run_gpu(case, dev, 32, tensors=d, stream=s)
+    assert flags == 0
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert np.array_equal(a.view(np.uint16), c.view(np.uint16))
+
+
+def test_library_allocated_workspace(dev):
+    case = _ragged("alloc", [3, 300, 1500, 77], H=4)
+    a, f1, d = run_gpu(case, dev)
+    b, f2, _ = run_gpu(case, dev, tensors=d, allocate_in_library=True)
+    assert f1 == 0 and f2 == 0
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_counters_return_to_zero_across_shapes(dev):
+    """One counter buffer serves calls of different sizes: every call leaves
+    it all zero, and partial results never land in it."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    cases = [_ragged("ws1", [1000, 2000, 5, 333], H=4, seed=1),
+             _ragged("ws2", [3000, 17, 900, 1, 64, 2500, 700, 1200], H=8, seed=2),
+             _ragged("ws3", [100, 2000], H=2, seed=3)]
+    ctr = torch.zeros(1 << 14, dtype=torch.int32, device=dev)
+    ws = torch.full((1 << 24,), 0x7F, dtype=torch.uint8, device=dev)   # garbage scratch
+    for rep in range(2):
+        for case in cases:
+            d = upload(case, dev)
+            out = torch.empty(case.q.shape, dtype=torch.float16, device=dev)
+            pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                      d["context_lens"], case.scale, partition_tokens=64, workspace=ws,
+                      counters=ctr)
+            assert pa.device_errors() == 0
+            assert int(ctr.abs().sum()) == 0
+            assert_parity(out.cpu().numpy(), oracle.decode_case(case), f"{case.name} rep {rep}")
+
+
+def test_many_sequences(dev):
+    rng = np.random.default_rng(3)
+    case = _ragged("many", rng.integers(0, 40, size=3000), H=2, D=64)
+    got, flags, _ = run_gpu(case, dev)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), "3000 sequences")
+
+
+def test_empty_batch(dev):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    z = torch.zeros((0, 2, 64), dtype=torch.float16, device=dev)
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.float16, device=dev)
+    pa.decode(z, z, kc, kc, torch.zeros((0, 3), dtype=torch.int32, device=dev),
+              torch.zeros((0,), dtype=torch.int32, device=dev), 0.125)
+    assert pa.device_errors() == 0
+
+
+# ----------------------------------------------------------------------------
+# reshape_and_cache: bit-exact
+# ----------------------------------------------------------------------------
+
+def test_reshape_and_cache_bit_exact(dev):
+    import paged_kv_cache_269_gb300 as pa
+    case = _ragged("rc", [5, 16, 17, 200, 1], H=4, new_tokens=True)
+    slots = case.slot_mapping.copy()
+    slots[1] = -1                                      # skipped
+    slots[2] = 0                                       # first slot of the pool
+    slots[3] = case.num_blocks * case.block_size - 1   # last slot of the pool
+    case.slot_mapping = slots
+    d = upload(case, dev)
+    pa.reshape_and_cache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    assert pa.device_errors() == 0
+    ref_k, ref_v = oracle.reshape_and_cache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                            slots)
+    assert np.array_equal(d["k_cache"].cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(d["v_cache"].cpu().numpy().view(np.uint16), ref_v.view(np.uint16))
+
+
+# ----------------------------------------------------------------------------
+# device-side range checks: reported, never a fault
+# ----------------------------------------------------------------------------
+
+def test_bad_table_entry_is_reported(dev):
+    import paged_kv_cache_269_gb300 as pa
+    case = _ragged("badtab", [40, 40], H=2)
+    tables = case.block_tables.copy()
+    tables[0, 1] = case.num_blocks + 5
+    case.block_tables = tables
+    got, flags, _ = run_gpu(case, dev)
+    assert flags & pa.DEVERR_TABLE
+    pa.reset_workspaces()
+    ok = _ragged("ok", [40, 40], H=2)
+    got2, flags2, _ = run_gpu(ok, dev)
+    assert flags2 == 0
+    assert_parity(got2, oracle.decode_case(ok), "after a reported error")
+
+
+def test_bad_context_len_is_reported(dev):
+    import paged_kv_cache_269_gb300 as pa
+    case = _ragged("badctx", [40, 20], H=2)
+    lens = case.context_lens.copy()
+    lens[1] = case.max_blocks_per_seq * case.block_size + 100
+    case.context_lens = lens
+    _, flags, _ = run_gpu(case, dev)
+    assert flags & pa.DEVERR_CONTEXT
+    pa.reset_workspaces()
+
+
+def test_bad_slot_is_reported(dev):
+    import paged_kv_cache_269_gb300 as pa
+    case = _ragged("badslot", [5, 9], H=2, new_tokens=True)
+    d = upload(case, dev)
+    before = d["k_cache"].cpu().numpy().copy()
+    import torch
+    bad = torch.tensor([case.num_blocks * case.block_size, -3], dtype=torch.int32, device=dev)
+    pa.reshape_and_cache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], bad)
+    assert pa.device_errors() & pa.DEVERR_SLOT
+    assert np.array_equal(d["k_cache"].cpu().numpy().view(np.uint16), before.view(np.uint16))
+
+
+# ----------------------------------------------------------------------------
+# the five workloads at full size, in the launch configuration the bench uses
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx"])
+def test_workload_full_size(dev, kind):
+    case = workloads.make_workload(kind)
+    got, flags, d = run_gpu(case, dev)
+    assert flags == 0
+    if kind == "shared_prefix":
+        dup = workloads.duplicate_prefix(case)
+        ref = oracle.decode_case(dup)          # the duplicated-prefix oracle
+        got_dup, flags2, _ = run_gpu(dup, dev)
+        assert flags2 == 0
+        # same arithmetic in the same order: bit-identical on the GPU too
+        assert np.array_equal(got.view(np.uint16), got_dup.view(np.uint16))
+    else:
+        ref = oracle.decode_case(case)
+    assert_parity(got, ref, kind)
+    if case.num_new_tokens:
+        # reshape_and_cache at full size: both caches bit-exact
+        ref_k, ref_v = oracle.reshape_and_cache(case.k_new, case.v_new, case.k_cache,
+                                                case.v_cache, case.slot_mapping)
+        assert np.array_equal(d["k_cache"].cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
+        assert np.array_equal(d["v_cache"].cpu().numpy().view(np.uint16), ref_v.view(np.uint16))

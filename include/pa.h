@@ -177,6 +177,44 @@ int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_ca
                  void *workspace, size_t workspace_bytes, uint32_t *counters,
                  size_t counters_bytes, void *stream);
 
+/* Capacity of the scratch array pa_decode_static uses instead of allocating. */
+#define PA_STATIC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB per device */
+
+/*
+ * pa_decode_static -- pa_decode that allocates no device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot let a library call cudaMalloc -- a serving process that reserves
+ * nearly all device memory for its KV-block pool up front and forbids later
+ * allocations, a latency-critical decode loop that must not stall on
+ * cudaMalloc / cudaFree (both may synchronise the device), or a plugin in a
+ * host program whose allocator it does not control.  The caller passes the
+ * same inputs and output as pa_decode; the split-context counters and partial
+ * results live in a fixed per-device array of PA_STATIC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until exit.
+ *
+ *   Arguments, layouts and results: as pa_decode.  Outputs match pa_decode
+ *   within the decode tolerance (the partition length may differ, see below).
+ *   Set-up: the first call on a device, made with that device current, looks
+ *   up the array's device address (cudaGetSymbolAddress); make that first
+ *   call before any stream capture.
+ *   Every call zeroes the array's counter area with cudaMemsetAsync on
+ *   `stream` and then launches the decode kernel; no cudaMalloc, cudaFree or
+ *   other allocating call is made.
+ *   Partition length: the pa_decode default when its partial results fit in
+ *   the array, otherwise the smallest power-of-two multiple of 512 tokens
+ *   that fits, or one pass over each whole context (no partials).
+ *   Limits: returns PA_ERR_WORKSPACE, launching nothing, when the counters
+ *   alone (8 + 4 * num_seqs * num_heads bytes, rounded up to 256) exceed
+ *   PA_STATIC_SCRATCH_BYTES.
+ *   Concurrency: all calls on a device share the one array, so calls whose
+ *   kernels may overlap on the GPU (different streams, or other host threads)
+ *   race and corrupt each other's results; serialise them.
+ */
+int pa_decode_static(void *out, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, const int32_t *context_lens, float scale,
+                     int32_t max_blocks_per_seq, const pa_dims *dims, void *stream);
+
 /*
  * Wait for `stream`, then return (in *flags, host) and clear the current
  * device's error word: an OR of PA_DEVERR_* bits set by kernels since the last

@@ -33,8 +33,8 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_UNSUPPO
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_bytes",
-           "pa_decode_counters_bytes", "pa_decode_ws", "pa_device_errors", "pa_status_string",
-           "pa_last_cuda_error", "pa_version")
+           "pa_decode_counters_bytes", "pa_decode_ws", "pa_decode_static", "pa_device_errors",
+           "pa_status_string", "pa_last_cuda_error", "pa_version")
 _SIZE_ERROR = (1 << 64) - 1
 
 
@@ -65,6 +65,8 @@ def _declare(l):
     l.pa_decode_counters_bytes.restype = sz
     l.pa_decode_ws.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, i32, vp, sz, vp,
                                sz, vp]
+    l.pa_decode_static.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp]
+    l.pa_decode_static.restype = ctypes.c_int
     l.pa_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     l.pa_status_string.argtypes = [ctypes.c_int]
     l.pa_status_string.restype = ctypes.c_char_p

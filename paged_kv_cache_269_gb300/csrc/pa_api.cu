@@ -97,6 +97,8 @@ int partition_plan(const pa_dims *dims, int32_t max_blocks_per_seq, int32_t part
 
 }  // namespace
 
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 void workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t max_parts,
                       WorkspaceLayout *out) {
     const size_t pairs = static_cast<size_t>(num_seqs) * static_cast<size_t>(num_heads);

@@ -45,6 +45,9 @@ struct WorkspaceLayout {
 void workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t max_parts,
                       WorkspaceLayout *out);
 
+// Record a CUDA error for pa_last_cuda_error() and return PA_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // Kernel launchers (pa_decode.cu / pa_cache.cu).  They return a cudaError_t.
 // `num_sms` sizes the persistent decode grid.
 cudaError_t launch_decode(const DecodeArgs &args, int head_dim, int block_size, int num_sms,

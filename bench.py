@@ -44,8 +44,8 @@ DECODE_SOURCES = ("paged_kv_cache_269_gb300/csrc/pa_decode.cu",
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="llama7b_b64", choices=workloads.WORKLOADS)
     p.add_argument("--partition-tokens", type=int, default=0)
@@ -99,58 +99,74 @@ def recorded_traffic(workload):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """nvidia-smi clock / throttle samples every 50 ms; summary() keeps the
+    samples whose nvidia-smi timestamp falls inside a time window."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.samples = []
+        self.thread = None
 
-    def __enter__(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.samples.append((time.time(), line))
+
+    def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
-        return self
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
 
-    def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
 
-    def summary(self):
-        if not getattr(self, "lines", None):
-            return None
+    def summary(self, t0, t1):
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        import datetime
+        for arrival, l in self.samples:
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                t = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = arrival
+            if not (t0 <= t <= t1):
+                continue
+            try:
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, f[5:9]):
+            for name, val in zip(names, f[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": "timed region"}
 
 
 # ----------------------------------------------------------------------------
@@ -268,20 +284,23 @@ def run_native(args, rank, world, local_rank):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local_rank) if not args.no_clocks else None
     if sampler:
-        sampler.__enter__()
+        sampler.start()
         time.sleep(0.3)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    t_begin = time.time()
     start.record(stream)
     for i in range(args.steps):
         step(d, evs[i])
     end.record(stream)
     torch.cuda.synchronize(dev)
+    t_end = time.time()
     if dist:
         dist.barrier()
     if sampler:
-        sampler.__exit__(None, None, None)
+        time.sleep(0.1)
+        sampler.stop()
     step_ms = start.elapsed_time(end) / args.steps
     decode_ms_each = [a.elapsed_time(b) for a, b in evs]
     decode_ms = sum(decode_ms_each) / len(decode_ms_each)
@@ -359,7 +378,7 @@ def run_native(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
-        "clocks": sampler.summary() if sampler else None,
+        "clocks": sampler.summary(t_begin, t_end) if sampler else None,
     }
     print(json.dumps(line))
 

@@ -20,7 +20,7 @@ __device__ unsigned int g_device_error_word = 0;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kDefaultPartitionTokens = 256;
+constexpr int kDefaultPartitionTokens = 512;
 constexpr int kVersion = 10000;  // 1.0.0
 
 struct DeviceState {

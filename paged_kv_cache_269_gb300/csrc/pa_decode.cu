@@ -43,16 +43,31 @@ constexpr unsigned kFull = 0xffffffffu;
 
 constexpr int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
+// Launch-shape constants, overridable at build time for tuning sweeps.
+// Several small CTAs per SM, each with its own producer warp, keep more
+// copies in flight than one large CTA: on the LLaMA-7B batch, 4 consumer
+// warps with a 40 KiB ring (4 CTAs per SM) ran 1.7x faster than 16 consumer
+// warps with a 176 KiB ring (1 CTA per SM).
+#ifndef PA_DECODE_CONSUMER_WARPS
+#define PA_DECODE_CONSUMER_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGE_KIB
+#define PA_DECODE_STAGE_KIB 40
+#endif
+#ifndef PA_DECODE_MAX_STAGES
+#define PA_DECODE_MAX_STAGES 16
+#endif
+
 template <int D, int B>
 struct Cfg {
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
     static_assert(B == 8 || B == 16 || B == 32, "block_size");
-    static constexpr int NC = 8;                      // consumer warps
+    static constexpr int NC = PA_DECODE_CONSUMER_WARPS;  // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;     // + one producer warp
     static constexpr int TILE_BYTES = B * D * 2;      // one K (or V) tile, fp16
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int STAGE_BUDGET = 80 * 1024;
-    static constexpr int NS = clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, 16);
+    static constexpr int STAGE_BUDGET = PA_DECODE_STAGE_KIB * 1024;
+    static constexpr int NS = clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, PA_DECODE_MAX_STAGES);
     static constexpr int ND = 4;                      // unit descriptor slots
     // q.k layout: LPT lanes per token, 8 dims (16 bytes) per lane.
     static constexpr int LPT = D / 8;
@@ -76,8 +91,10 @@ struct Cfg {
     static constexpr int OFF_FLAGS = OFF_BARS + NUM_BARS * 8;
     static constexpr int OFF_SEQ = OFF_FLAGS + 16;    // prefix[S + 1], ctx[S]
 
-    // Two CTAs per SM when the shared-memory footprint allows it.
-    static constexpr int MIN_BLOCKS = (OFF_SEQ + 4096 <= 110 * 1024) ? 2 : 1;
+    // CTAs per SM the shared-memory footprint allows (228 KiB per SM, 1 KiB
+    // reserved per CTA, room for 1024 sequences); the launch bound caps the
+    // registers so that as many CTAs fit.
+    static constexpr int MIN_BLOCKS = clamp_int(228 * 1024 / (OFF_SEQ + 8 * 1024 + 1024), 1, 8);
 
     static size_t smem_bytes(int num_seqs) {
         return static_cast<size_t>(OFF_SEQ) + (2 * static_cast<size_t>(num_seqs) + 1) * 4;

@@ -73,14 +73,16 @@ def test_split_case_matches_regular_entry_point(dev):
 
 
 def test_partition_grows_to_fit_the_array(dev):
-    # 64 x 32 pairs with 256-block table rows: the default partition's partial
-    # results (about 17 MB) do not fit the 16 MiB array, so a longer partition
-    # is used; four long contexts still need several partitions each.
+    # 64 x 32 pairs with 512-block table rows: the default 512-token
+    # partition's partial results (16 partitions, about 17 MB) do not fit the
+    # 16 MiB array, so a longer partition is used; four long contexts still
+    # need several partitions each.
+    import paged_kv_cache_269_gb300 as pa
     rng = np.random.default_rng(31)
     lens = np.concatenate([rng.integers(1, 600, size=60), np.full(4, 4096)])
     case = workloads.build_case("static_grow", lens, num_heads=32, head_dim=128, seed=31,
-                                max_blocks_per_seq=256)
-    default_partials = 64 * 32 * 16 * (128 + 2) * 4
+                                max_blocks_per_seq=512)
+    default_partials = pa.decode_workspace_bytes(64, 32, 128, 16, case.num_blocks, 512)
     assert default_partials > STATIC_SCRATCH_BYTES
     _check_against_regular(case, dev)
 

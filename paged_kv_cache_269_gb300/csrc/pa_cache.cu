@@ -6,6 +6,10 @@
 // encoding (slot = physical_block * B + offset, negative = skip) is this
 // library's reading.
 //
+// Launched with programmatic dependent launch: it may become resident while the
+// previous decode on the stream drains, and waits for it before touching the
+// caches.
+//
 // A pure copy: one thread moves 16 bytes (8 fp16 values) of one (token, head)
 // row of K and the same of V; a warp covers whole 256-byte rows, so loads and
 // stores are fully coalesced.  The work is a few MiB per decode step, so the
@@ -23,6 +27,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     uint4 *__restrict__ v_cache, const int32_t *__restrict__ slot_mapping, int32_t num_tokens,
     int32_t num_heads, int32_t chunks_per_row, int32_t block_size, long long pool_slots,
     unsigned int *err) {
+    // The previous kernel on the stream may still be reading the caches.
+    allow_dependents_to_launch();
+    grid_dependency_wait();
     const long long total = static_cast<long long>(num_tokens) * num_heads * chunks_per_row;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -59,12 +66,21 @@ cudaError_t launch_reshape_and_cache(const uint16_t *k, const uint16_t *v, uint1
     const int threads = 256;
     long long blocks = (total + threads - 1) / threads;
     if (blocks > 65535) blocks = 65535;
-    reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
-        reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), slot_mapping,
-        num_tokens, num_heads, chunks, block_size,
-        static_cast<long long>(num_blocks) * block_size, err);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel,
+                              reinterpret_cast<const uint4 *>(k), reinterpret_cast<const uint4 *>(v),
+                              reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
+                              slot_mapping, num_tokens, num_heads, chunks, block_size,
+                              static_cast<long long>(num_blocks) * block_size, err);
 }
 
 }  // namespace pa

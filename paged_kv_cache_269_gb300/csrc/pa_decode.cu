@@ -47,15 +47,19 @@ constexpr int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? 
 // Several small CTAs per SM, each with its own producer warp, keep more
 // copies in flight than one large CTA: on the LLaMA-7B batch, 4 consumer
 // warps with a 40 KiB ring (4 CTAs per SM) ran 1.7x faster than 16 consumer
-// warps with a 176 KiB ring (1 CTA per SM).
+// warps with a 176 KiB ring (1 CTA per SM).  Two descriptor slots instead of
+// four free the shared memory for a sixth ring stage at 4 CTAs per SM.
 #ifndef PA_DECODE_CONSUMER_WARPS
 #define PA_DECODE_CONSUMER_WARPS 4
 #endif
 #ifndef PA_DECODE_STAGE_KIB
-#define PA_DECODE_STAGE_KIB 40
+#define PA_DECODE_STAGE_KIB 48
 #endif
 #ifndef PA_DECODE_MAX_STAGES
 #define PA_DECODE_MAX_STAGES 16
+#endif
+#ifndef PA_DECODE_DESC_SLOTS
+#define PA_DECODE_DESC_SLOTS 2
 #endif
 
 template <int D, int B>
@@ -68,7 +72,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int STAGE_BUDGET = PA_DECODE_STAGE_KIB * 1024;
     static constexpr int NS = clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, PA_DECODE_MAX_STAGES);
-    static constexpr int ND = 4;                      // unit descriptor slots
+    static constexpr int ND = PA_DECODE_DESC_SLOTS;   // unit descriptor slots
     // q.k layout: LPT lanes per token, 8 dims (16 bytes) per lane.
     static constexpr int LPT = D / 8;
     static constexpr int TPR = 32 / LPT;              // tokens per row group
@@ -296,6 +300,10 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         *abort_flag = 0;
         mbar_init_fence();
     }
+    // Everything above touched shared memory only; inputs may still be being
+    // written by the previous kernel on the stream (e.g. reshape_and_cache).
+    grid_dependency_wait();
+    allow_dependents_to_launch();
     const int ctx_cap = a.max_blocks_per_seq * B;
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         int c = a.context_lens[s];
@@ -620,8 +628,17 @@ cudaError_t launch_decode(const DecodeArgs &args, int head_dim, int block_size, 
     if (grid > max_units) grid = max_units;
     if (grid < 1) grid = 1;
     void *params[] = {const_cast<DecodeArgs *>(&args)};
-    return cudaLaunchKernel(v->kernel, dim3(static_cast<unsigned>(grid)), dim3(v->threads), params,
-                            smem, stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(v->threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, v->kernel, params);
 }
 
 }  // namespace pa

@@ -151,6 +151,20 @@ __device__ __forceinline__ uint64_t make_l2_policy_evict_last() {
     return policy;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream is still
+// running; grid_dependency_wait() blocks until that kernel has completed and
+// its memory is visible, and must precede every global-memory access that
+// could depend on it.  allow_dependents_to_launch() lets the next such kernel
+// become resident early (it still waits for this one to finish).  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents_to_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Global loads that bypass L1: used for partial results written by other CTAs
 // of the same launch.
 __device__ __forceinline__ float2 ld_cg_f2(const float2 *p) { return __ldcg(p); }

@@ -232,3 +232,28 @@ def test_workload_full_size(dev, kind):
                                                 case.v_cache, case.slot_mapping)
         assert np.array_equal(d["k_cache"].cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
         assert np.array_equal(d["v_cache"].cpu().numpy().view(np.uint16), ref_v.view(np.uint16))
+
+
+def test_back_to_back_steps_keep_their_order(dev):
+    """Steps issued without any host synchronisation (reshape_and_cache then
+    decode, repeated; both kernels use programmatic dependent launch) must
+    each see their own step's new tokens: the new K/V alternate between two
+    sets and every step's output is checked against the oracle for its set."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    base = _ragged("b2b", [300, 17, 1024, 640, 1, 2000], H=4, new_tokens=True, seed=11)
+    alt = _ragged("b2b", [300, 17, 1024, 640, 1, 2000], H=4, new_tokens=True, seed=11)
+    workloads.fill_normal_f16(alt.k_new, 99, 4)
+    workloads.fill_normal_f16(alt.v_new, 99, 5)
+    refs = [oracle.decode_case(base), oracle.decode_case(alt)]
+    d = upload(base, dev)
+    news = [(d["k_new"], d["v_new"]), (upload(alt, dev)["k_new"], upload(alt, dev)["v_new"])]
+    outs = [torch.empty(base.q.shape, dtype=torch.float16, device=dev) for _ in range(12)]
+    for i, out in enumerate(outs):
+        kn, vn = news[i % 2]
+        pa.reshape_and_cache(kn, vn, d["k_cache"], d["v_cache"], d["slot_mapping"])
+        pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                  base.scale, partition_tokens=256)
+    assert pa.device_errors() == 0
+    for i, out in enumerate(outs):
+        assert_parity(out.cpu().numpy(), refs[i % 2], f"step {i}")

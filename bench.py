@@ -54,6 +54,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--flush-l2", action="store_true",
+                   help="write a 256 MiB buffer before every step so shared blocks start cold; "
+                        "step time then sums per-step events and excludes the flush")
     return p.parse_args()
 
 
@@ -227,8 +230,10 @@ def config_of(case, args):
             "num_blocks": case.num_blocks, "max_blocks_per_seq": case.max_blocks_per_seq,
             "total_context_tokens": int(case.context_lens.sum()),
             "new_tokens": case.num_new_tokens,
-            "l2": "inputs larger than L2 (no flush)" if 2 * case.k_cache.nbytes > L2_BYTES
-            else "inputs smaller than L2",
+            "l2": ("flushed before every step (256 MiB write, excluded from the step time)"
+                   if getattr(args, "flush_l2", False) else
+                   "inputs larger than L2 (no flush)" if 2 * case.k_cache.nbytes > L2_BYTES
+                   else "inputs smaller than L2"),
             "parallelism": f"dp{args.gpus} (replicas)", "seed": case.seed}
 
 
@@ -258,7 +263,14 @@ def run_native(args, rank, world, local_rank):
                       dtype=torch.int32, device=dev)
     torch.cuda.synchronize(dev)
 
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
+
     def step(ins, ev=None):
+        if flush_buf is not None:
+            with torch.cuda.stream(stream):
+                flush_buf.fill_(1)
+        if ev is not None and len(ev) > 2:
+            ev[2].record(stream)
         pa.reshape_and_cache(ins["k_new"], ins["v_new"], d["k_cache"], d["v_cache"],
                              ins["slot_mapping"], stream=stream)
         if ev is not None:
@@ -279,7 +291,8 @@ def run_native(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    nev = 3 if args.flush_l2 else 2
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(nev))
            for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local_rank) if not args.no_clocks else None
@@ -302,7 +315,9 @@ def run_native(args, rank, world, local_rank):
         time.sleep(0.1)
         sampler.stop()
     step_ms = start.elapsed_time(end) / args.steps
-    decode_ms_each = [a.elapsed_time(b) for a, b in evs]
+    if args.flush_l2:  # per-step events around reshape + decode, flush excluded
+        step_ms = sum(e[2].elapsed_time(e[1]) for e in evs) / args.steps
+    decode_ms_each = [e[0].elapsed_time(e[1]) for e in evs]
     decode_ms = sum(decode_ms_each) / len(decode_ms_each)
     if pa.device_errors(stream=stream):
         raise RuntimeError("device error during the timed steps")
@@ -363,6 +378,7 @@ def run_native(args, rank, world, local_rank):
         return
     peak, peak_kind = measured_peaks()
     dec_bytes = workloads.decode_algorithmic_bytes(case)
+    uniq_bytes = workloads.decode_unique_bytes(case)
     achieved = dec_bytes / (decode_ms * 1e-3) / 1e9
     value = world * step_bytes(case) / (step_ms * 1e-3) / 1e9
     cpu = None
@@ -386,6 +402,8 @@ def run_native(args, rank, world, local_rank):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": "pa_decode", "algorithmic_bytes_per_launch": int(dec_bytes),
+                     "unique_bytes_per_launch": int(uniq_bytes),
+                     "achieved_unique": round(uniq_bytes / (decode_ms * 1e-3) / 1e9, 2),
                      "traffic": recorded_traffic(args.workload)},
         "cpu_baseline": cpu,
         "e2e": e2e,

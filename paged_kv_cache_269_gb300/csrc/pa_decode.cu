@@ -58,6 +58,9 @@ constexpr int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? 
 #ifndef PA_DECODE_MAX_STAGES
 #define PA_DECODE_MAX_STAGES 16
 #endif
+#ifndef PA_DECODE_MIXED_FMA
+#define PA_DECODE_MIXED_FMA 1
+#endif
 #ifndef PA_DECODE_DESC_SLOTS
 #define PA_DECODE_DESC_SLOTS 2
 #endif
@@ -110,73 +113,119 @@ __device__ __forceinline__ float2 h2f(uint32_t bits) {
     return __half22float2(h);
 }
 
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Partial q.k over this lane's 8 dims of one K row (16 bytes).
+__device__ __forceinline__ float dot8(const uint4 kv, const uint4 qh, const float (&qf)[8]) {
+#if PA_DECODE_MIXED_FMA
+    // fp16 x fp16 products are exact in fp32, so fusing the conversion into
+    // the FMA gives the same result as converting first.
+    float dot = 0.f;
+    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+    const uint32_t qw[4] = {qh.x, qh.y, qh.z, qh.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+            "mov.b32 {a0, a1}, %1;\n\t"
+            "mov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+            "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+            : "+f"(dot)
+            : "r"(kw[i]), "r"(qw[i]));
+    return dot;
+#else
+    (void)qh;
+    const float2 k0 = h2f(kv.x), k1 = h2f(kv.y), k2 = h2f(kv.z), k3 = h2f(kv.w);
+    float dot = qf[0] * k0.x;
+    dot = fmaf(qf[1], k0.y, dot);
+    dot = fmaf(qf[2], k1.x, dot);
+    dot = fmaf(qf[3], k1.y, dot);
+    dot = fmaf(qf[4], k2.x, dot);
+    dot = fmaf(qf[5], k2.y, dot);
+    dot = fmaf(qf[6], k3.x, dot);
+    dot = fmaf(qf[7], k3.y, dot);
+    return dot;
+#endif
+}
+
 // One KV tile of one unit, processed by one warp.
 template <int D, int B>
 __device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t *vtile,
-                                             const float (&qf)[8], float scale_log2, int nvalid,
-                                             float &run_max, float &run_sum,
-                                             float (&acc)[Cfg<D, B>::DPL], float *probs,
-                                             int lane) {
+                                             const uint4 qh, const float (&qf)[8],
+                                             float scale_log2, int nvalid, float &run_max,
+                                             float &run_sum, float (&acc)[Cfg<D, B>::DPL],
+                                             float *probs, int lane) {
     using C = Cfg<D, B>;
     const int c = lane % C::LPT;   // 16-byte column of the row
     const int tr = lane / C::LPT;  // token within the row group
 
-    // scores: partial dot products over this lane's 8 dims
+    // partial dot products over this lane's 8 dims, one per row group
     float sc[C::RG];
     const uint4 *K4 = reinterpret_cast<const uint4 *>(ktile);
 #pragma unroll
-    for (int r = 0; r < C::RG; ++r) {
-        const uint4 kv = K4[(r * C::TPR + tr) * C::LPT + c];
-        const float2 k0 = h2f(kv.x), k1 = h2f(kv.y), k2 = h2f(kv.z), k3 = h2f(kv.w);
-        float dot = qf[0] * k0.x;
-        dot = fmaf(qf[1], k0.y, dot);
-        dot = fmaf(qf[2], k1.x, dot);
-        dot = fmaf(qf[3], k1.y, dot);
-        dot = fmaf(qf[4], k2.x, dot);
-        dot = fmaf(qf[5], k2.y, dot);
-        dot = fmaf(qf[6], k3.x, dot);
-        dot = fmaf(qf[7], k3.y, dot);
-        sc[r] = dot;
+    for (int r = 0; r < C::RG; ++r) sc[r] = dot8(K4[(r * C::TPR + tr) * C::LPT + c], qh, qf);
+
+    // Reduce-scatter across the LPT lanes of a token.  Each halving step swaps
+    // half of a lane's remaining partial sums with the lane `o` apart and adds
+    // the half it keeps, so after H steps a lane holds RG / 2^H rows summed
+    // over 2^H lanes (rows base .. base + V - 1); the lane bits still unsummed
+    // are finished with plain butterflies, after which those lanes hold equal
+    // copies.  This needs RG - 1 + log2 shuffles instead of RG * log2(LPT).
+    constexpr int H = ilog2(C::RG < C::LPT ? C::RG : C::LPT);
+    constexpr int V = C::RG >> H;
+    constexpr int DUP = C::LPT >> H;  // lanes holding the same rows
+    int base = 0;
+#pragma unroll
+    for (int step = 0; step < H; ++step) {
+        const int o = C::LPT >> (step + 1);
+        const int half = (C::RG >> step) / 2;
+        const bool upper = (c & o) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+            const float send = upper ? sc[j] : sc[j + half];
+            const float keep = upper ? sc[j + half] : sc[j];
+            sc[j] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+        base += upper ? half : 0;
     }
 #pragma unroll
-    for (int r = 0; r < C::RG; ++r) {
+    for (int o = DUP / 2; o >= 1; o >>= 1) {
 #pragma unroll
-        for (int off = C::LPT / 2; off >= 1; off >>= 1)
-            sc[r] += __shfl_xor_sync(kFull, sc[r], off);
+        for (int j = 0; j < V; ++j) sc[j] += __shfl_xor_sync(kFull, sc[j], o);
     }
 
     // scale into the log2 domain, mask the tokens past the context, tile max
     float tile_max = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < C::RG; ++r) {
-        const int t = r * C::TPR + tr;
-        sc[r] = (t < nvalid) ? sc[r] * scale_log2 : -INFINITY;
-        tile_max = fmaxf(tile_max, sc[r]);
+    for (int j = 0; j < V; ++j) {
+        const int t = (base + j) * C::TPR + tr;
+        sc[j] = (t < nvalid) ? sc[j] * scale_log2 : -INFINITY;
+        tile_max = fmaxf(tile_max, sc[j]);
     }
 #pragma unroll
-    for (int off = C::LPT; off < 32; off <<= 1)
-        tile_max = fmaxf(tile_max, __shfl_xor_sync(kFull, tile_max, off));
+    for (int o = 16; o >= DUP; o >>= 1)
+        tile_max = fmaxf(tile_max, __shfl_xor_sync(kFull, tile_max, o));
 
     // online softmax update
     const float new_max = fmaxf(run_max, tile_max);
     const float alpha = exp2f(run_max - new_max);
     float psum = 0.f;
 #pragma unroll
-    for (int r = 0; r < C::RG; ++r) {
-        sc[r] = exp2f(sc[r] - new_max);
-        psum += sc[r];
+    for (int j = 0; j < V; ++j) {
+        sc[j] = exp2f(sc[j] - new_max);
+        psum += sc[j];
     }
 #pragma unroll
-    for (int off = C::LPT; off < 32; off <<= 1) psum += __shfl_xor_sync(kFull, psum, off);
+    for (int o = 16; o >= DUP; o >>= 1) psum += __shfl_xor_sync(kFull, psum, o);
     run_sum = run_sum * alpha + psum;
     run_max = new_max;
 #pragma unroll
     for (int i = 0; i < C::DPL; ++i) acc[i] *= alpha;
 
-    // publish the B probabilities to the whole warp
-    if (c == 0) {
+    // publish the B probabilities to the whole warp (one writer per token)
+    if ((c & (DUP - 1)) == 0) {
 #pragma unroll
-        for (int r = 0; r < C::RG; ++r) probs[r * C::TPR + tr] = sc[r];
+        for (int j = 0; j < V; ++j) probs[(base + j) * C::TPR + tr] = sc[j];
     }
     __syncwarp();
 
@@ -450,9 +499,9 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         const int h = m[1], p = m[2], nt = m[3], ctx = m[4], np = m[5];
 
         float qf[8];
+        const uint4 qraw =
+            *reinterpret_cast<const uint4 *>(desc_q + slot * D + (lane % C::LPT) * 8);
         {
-            const uint4 qraw =
-                *reinterpret_cast<const uint4 *>(desc_q + slot * D + (lane % C::LPT) * 8);
             const float2 q0 = h2f(qraw.x), q1 = h2f(qraw.y), q2 = h2f(qraw.z), q3 = h2f(qraw.w);
             qf[0] = q0.x; qf[1] = q0.y; qf[2] = q1.x; qf[3] = q1.y;
             qf[4] = q2.x; qf[5] = q2.y; qf[6] = q3.x; qf[7] = q3.y;
@@ -472,8 +521,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                 const int tok0 = (p * TPU + j) * B;
                 const int nvalid = min(B, ctx - tok0);
                 const uint8_t *ktile = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
-                consume_tile<D, B>(ktile, ktile + C::TILE_BYTES, qf, a.scale_log2, nvalid, run_max,
-                                   run_sum, acc, probs, lane);
+                consume_tile<D, B>(ktile, ktile + C::TILE_BYTES, qraw, qf, a.scale_log2, nvalid,
+                                   run_max, run_sum, acc, probs, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);

@@ -18,8 +18,9 @@
  *  - All work is enqueued on `stream` (a cudaStream_t; NULL means the legacy
  *    default stream) and runs asynchronously: a PA_OK return means the launch
  *    succeeded, not that the kernel has finished.
- *  - fp16 tensors are IEEE binary16, row-major and contiguous in the shapes
- *    given; every fp16 device pointer must be 16-byte aligned.
+ *  - 16-bit tensors (fp16 or bf16, per pa_dims.dtype) are row-major and
+ *    contiguous in the shapes given; every such device pointer must be
+ *    16-byte aligned.
  *  - Errors found on the host return a negative pa_status and launch nothing.
  *    Errors only the device can see (a block-table entry or slot outside the
  *    pool, a context length outside [0, max_blocks_per_seq * block_size]) are
@@ -53,12 +54,22 @@ typedef enum pa_status {
 #define PA_DEVERR_SLOT    0x4u  /* a slot_mapping entry was >= num_blocks * block_size      */
 #define PA_DEVERR_TIMEOUT 0x8u  /* an internal pipeline wait gave up (should never happen) */
 
+/* Element type of q, the caches and the output (and of k, v for
+ * reshape_and_cache): IEEE binary16, or bfloat16 (the top 16 bits of an
+ * IEEE binary32).  The pages name both for the kernels (doramagic.ai vLLM
+ * manual, "PagedAttention V1 内核": FP16/BF16). */
+typedef enum pa_dtype {
+    PA_DTYPE_F16 = 0,
+    PA_DTYPE_BF16 = 1
+} pa_dtype;
+
 /* Sizes shared by both calls.
  *   num_seqs    S: sequences in the decode batch (>= 0)
  *   num_heads   H: attention heads; K/V heads equal query heads (no grouping)
  *   head_dim    D: 64, 128 or 256
  *   block_size  B: tokens per KV block: 8, 16 (the pages' default) or 32
  *   num_blocks  N: physical blocks in the cache pool (> 0)
+ *   dtype       a pa_dtype; a zero-initialised struct selects fp16
  * Cache layout [N, H, B, D] fp16: element (blk, h, t, d) is at
  * ((blk * H + h) * B + t) * D + d ("vLLM 2026 推理引擎全解", §2.2, the kernel
  * sketch's k_cache layout [num_pages, num_heads, page_size, head_dim]). */
@@ -68,6 +79,7 @@ typedef struct pa_dims {
     int32_t head_dim;
     int32_t block_size;
     int32_t num_blocks;
+    int32_t dtype;
 } pa_dims;
 
 /*

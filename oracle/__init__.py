@@ -61,13 +61,15 @@ def load(path: str = _LIB_PATH, src: str = _SRC):
     i32p = ctypes.POINTER(ctypes.c_int32)
     ci = ctypes.c_int
     lib.oracle_decode.argtypes = [dp, u16p, u16p, u16p, i32p, i32p, ctypes.c_double,
-                                  ci, ci, ci, ci, ci, ci]
+                                  ci, ci, ci, ci, ci, ci, ci]
     lib.oracle_decode.restype = ci
     lib.oracle_reshape_and_cache.argtypes = [u16p, u16p, u16p, u16p, i32p,
                                              ci, ci, ci, ci, ci]
     lib.oracle_reshape_and_cache.restype = ci
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_half_to_double.restype = ctypes.c_double
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_double.restype = ctypes.c_double
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ci
     return lib
@@ -100,10 +102,18 @@ def half_to_double(bits: int, lib=None) -> float:
     return (lib or _get()).oracle_half_to_double(int(bits))
 
 
+DTYPES = {"f16": 0, "bf16": 1}
+
+
+def bf16_to_double(bits: int, lib=None) -> float:
+    return (lib or _get()).oracle_bf16_to_double(int(bits))
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale,
-           lib=None) -> np.ndarray:
-    """fp64 attention output [S, H, D] for fp16 q [S, H, D] over a paged cache
-    [N, H, B, D] reached through block_tables [S, MB] and context_lens [S]."""
+           lib=None, dtype: str = "f16") -> np.ndarray:
+    """fp64 attention output [S, H, D] for q [S, H, D] over a paged cache
+    [N, H, B, D] reached through block_tables [S, MB] and context_lens [S].
+    dtype "f16": arrays are float16; "bf16": uint16 arrays of bfloat16 bits."""
     lib = lib or _get()
     S, H, D = q.shape
     N, H2, B, D2 = k_cache.shape
@@ -114,7 +124,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale,
     keep = [_u16(q), _u16(k_cache), _u16(v_cache), _i32(block_tables), _i32(context_lens)]
     rc = lib.oracle_decode(out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                            keep[0][1], keep[1][1], keep[2][1], keep[3][1], keep[4][1],
-                           float(scale), S, H, D, B, N, max(1, MB))
+                           float(scale), S, H, D, B, N, max(1, MB), DTYPES[dtype])
     if rc != 0:
         raise OracleError(ERRORS.get(rc, str(rc)))
     return out
@@ -128,8 +138,8 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, lib=None):
     N, H2, B, D2 = k_cache.shape
     if (H2, D2) != (H, D) or v.shape != k.shape or v_cache.shape != k_cache.shape:
         raise OracleError("shape mismatch")
-    kc = np.array(k_cache, dtype=np.float16, copy=True, order="C")
-    vc = np.array(v_cache, dtype=np.float16, copy=True, order="C")
+    kc = np.array(k_cache, copy=True, order="C")
+    vc = np.array(v_cache, copy=True, order="C")
     kk, vv, ss = _u16(k), _u16(v), _i32(slot_mapping)
     kcu, vcu = _u16(kc), _u16(vc)
     rc = lib.oracle_reshape_and_cache(kk[1], vv[1], kcu[1], vcu[1], ss[1], T, H, D, B, N)
@@ -144,4 +154,5 @@ def decode_case(case, lib=None) -> np.ndarray:
     kc, vc = case.k_cache, case.v_cache
     if case.slot_mapping is not None and case.num_new_tokens:
         kc, vc = reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping, lib=lib)
-    return decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale, lib=lib)
+    return decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale, lib=lib,
+                  dtype=case.dtype)

@@ -26,7 +26,7 @@
  *
  * So the oracle, per (sequence s, head h):
  *   1. gathers K_s, V_s (ctx_s x head_dim) through the block table, converting
- *      each fp16 value exactly to double;
+ *      each fp16 (or bf16) value exactly to double;
  *   2. scores_t = scale * sum_d q[d] * K_s[t][d];
  *   3. weights_t = exp(scores_t - max_t scores_t), normalised by their sum;
  *   4. out[d] = sum_t weights_t * V_s[t][d].
@@ -70,6 +70,24 @@ double oracle_half_to_double(uint16_t bits)
     return sign ? -magnitude : magnitude;
 }
 
+/* bfloat16 -> double, exactly: a bfloat16 is the upper 16 bits of an IEEE
+ * 754 binary32 (1 sign bit, 8 exponent bits, 7 fraction bits). */
+double oracle_bf16_to_double(uint16_t bits)
+{
+    uint32_t word = (uint32_t)bits << 16;
+    float value;
+    memcpy(&value, &word, sizeof value);
+    return (double)value;
+}
+
+#define ORACLE_F16 0
+#define ORACLE_BF16 1
+
+static double element_to_double(uint16_t bits, int dtype)
+{
+    return dtype == ORACLE_BF16 ? oracle_bf16_to_double(bits) : oracle_half_to_double(bits);
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
@@ -92,9 +110,10 @@ static size_t cache_index(int64_t block, int head, int offset, int dim,
  * Decode attention for every (sequence, head).
  *
  * out           [num_seqs, num_heads, head_dim] double (written)
- * q             [num_seqs, num_heads, head_dim] fp16 bits
- * k_cache       [num_blocks, num_heads, block_size, head_dim] fp16 bits
+ * q             [num_seqs, num_heads, head_dim] 16-bit element bits
+ * k_cache       [num_blocks, num_heads, block_size, head_dim] element bits
  * v_cache       same layout as k_cache
+ * dtype         0: elements are IEEE binary16; 1: bfloat16
  * block_tables  [num_seqs, max_blocks_per_seq] int32
  * context_lens  [num_seqs] int32
  *
@@ -105,10 +124,11 @@ int oracle_decode(double *out, const uint16_t *q, const uint16_t *k_cache,
                   const uint16_t *v_cache, const int32_t *block_tables,
                   const int32_t *context_lens, double scale, int num_seqs,
                   int num_heads, int head_dim, int block_size, int num_blocks,
-                  int max_blocks_per_seq)
+                  int max_blocks_per_seq, int dtype)
 {
     if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks < 0 || max_blocks_per_seq <= 0)
+        num_blocks < 0 || max_blocks_per_seq <= 0 ||
+        (dtype != ORACLE_F16 && dtype != ORACLE_BF16))
         return ORACLE_BAD_ARG;
 
     /* Check every input the computation will use before computing anything. */
@@ -156,12 +176,12 @@ int oracle_decode(double *out, const uint16_t *q, const uint16_t *k_cache,
             int offset = t % block_size;
             for (int d = 0; d < head_dim; ++d) {
                 size_t at = cache_index(phys, h, offset, d, num_heads, block_size, head_dim);
-                K[(size_t)t * head_dim + d] = oracle_half_to_double(k_cache[at]);
-                V[(size_t)t * head_dim + d] = oracle_half_to_double(v_cache[at]);
+                K[(size_t)t * head_dim + d] = element_to_double(k_cache[at], dtype);
+                V[(size_t)t * head_dim + d] = element_to_double(v_cache[at], dtype);
             }
         }
         for (int d = 0; d < head_dim; ++d)
-            qd[d] = oracle_half_to_double(q[(size_t)pair * head_dim + d]);
+            qd[d] = element_to_double(q[(size_t)pair * head_dim + d], dtype);
 
         /* Step 2: scaled scores. */
         double max_score = -INFINITY;

@@ -44,10 +44,14 @@ class PaError(RuntimeError):
         self.status = status
 
 
+DTYPE_F16 = 0
+DTYPE_BF16 = 1
+
+
 class Dims(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int32)]
+                ("num_blocks", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -137,20 +141,32 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _element_dtype(k_cache):
+    """The library dtype code of a cache tensor (fp16 or bf16)."""
+    torch = _torch()
+    if k_cache.dtype == torch.float16:
+        return DTYPE_F16
+    if k_cache.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"k_cache must be float16 or bfloat16, got {k_cache.dtype}")
+
+
 def _cache_dims(k_cache, num_seqs=0):
     N, H, B, D = k_cache.shape
-    return Dims(num_seqs, H, D, B, N)
+    return Dims(num_seqs, H, D, B, N, _element_dtype(k_cache))
 
 
 def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None):
     """k_cache[slot // B, :, slot % B, :] = k[i] (same for v) for every i with
     slot = slot_mapping[i] >= 0.  Caches are updated in place."""
     torch = _torch()
-    _need(k_cache, "k_cache", torch.float16, 4)
+    _element_dtype(k_cache)
+    et = k_cache.dtype
+    _need(k_cache, "k_cache", et, 4)
     dev = k_cache.device
-    _need(v_cache, "v_cache", torch.float16, 4, dev)
-    _need(k, "k", torch.float16, 3, dev)
-    _need(v, "v", torch.float16, 3, dev)
+    _need(v_cache, "v_cache", et, 4, dev)
+    _need(k, "k", et, 3, dev)
+    _need(v, "v", et, 3, dev)
     _need(slot_mapping, "slot_mapping", torch.int32, 1, dev)
     N, H, B, D = k_cache.shape
     T = k.shape[0]
@@ -166,9 +182,9 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None):
 
 
 def decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, num_blocks,
-                           max_blocks_per_seq, partition_tokens=0) -> int:
+                           max_blocks_per_seq, partition_tokens=0, dtype=DTYPE_F16) -> int:
     """Bytes of partial-result workspace pa_decode_ws needs (0: none)."""
-    dims = Dims(num_seqs, num_heads, head_dim, block_size, num_blocks)
+    dims = Dims(num_seqs, num_heads, head_dim, block_size, num_blocks, dtype)
     n = lib().pa_decode_workspace_bytes(ctypes.byref(dims), max_blocks_per_seq, partition_tokens)
     if n == _SIZE_ERROR:
         raise PaError(-2, "pa_decode_workspace_bytes: invalid sizes")
@@ -216,9 +232,10 @@ def reset_workspaces():
 def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
            max_blocks_per_seq=None, partition_tokens=0, workspace=None, counters=None,
            stream=None, allocate_in_library=False):
-    """Paged-attention decode into `out` [S, H, D] fp16.
+    """Paged-attention decode into `out` [S, H, D].
 
-    q [S, H, D] fp16; k_cache / v_cache [N, H, B, D] fp16; block_tables
+    q [S, H, D]; k_cache / v_cache [N, H, B, D], all float16 or all
+    bfloat16; block_tables
     [S, MB] int32; context_lens [S] int32.  partition_tokens = 0 picks the
     library default.  counters (a zeroed int32 CUDA tensor of at least
     decode_counters_bytes(...) bytes) and workspace (a uint8 CUDA tensor of at
@@ -227,11 +244,13 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
     which allocates both itself with cudaMallocAsync on the stream.
     """
     torch = _torch()
-    _need(k_cache, "k_cache", torch.float16, 4)
+    _element_dtype(k_cache)
+    et = k_cache.dtype
+    _need(k_cache, "k_cache", et, 4)
     dev = k_cache.device
-    _need(v_cache, "v_cache", torch.float16, 4, dev)
-    _need(q, "q", torch.float16, 3, dev)
-    _need(out, "out", torch.float16, 3, dev)
+    _need(v_cache, "v_cache", et, 4, dev)
+    _need(q, "q", et, 3, dev)
+    _need(out, "out", et, 3, dev)
     _need(block_tables, "block_tables", torch.int32, 2, dev)
     _need(context_lens, "context_lens", torch.int32, 1, dev)
     N, H, B, D = k_cache.shape

@@ -73,7 +73,8 @@ int check_dims(const pa_dims *dims, bool need_seqs) {
         dims->num_blocks <= 0)
         return PA_ERR_SHAPE;
     if (need_seqs && dims->num_seqs < 0) return PA_ERR_SHAPE;
-    if (!decode_variant_supported(dims->head_dim, dims->block_size)) return PA_ERR_UNSUPPORTED;
+    if (!decode_variant_supported(dims->dtype, dims->head_dim, dims->block_size))
+        return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 
@@ -206,7 +207,7 @@ int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_ca
     a.part_ml = parts > 1 ? reinterpret_cast<float *>(ws + l.ml_off) : nullptr;
     a.part_acc = parts > 1 ? reinterpret_cast<float *>(ws + l.acc_off) : nullptr;
     a.err = st->err;
-    cudaError_t e = launch_decode(a, dims->head_dim, dims->block_size, st->num_sms,
+    cudaError_t e = launch_decode(a, dims->dtype, dims->head_dim, dims->block_size, st->num_sms,
                                   static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidConfiguration) return PA_ERR_UNSUPPORTED;  // too many sequences
     return e == cudaSuccess ? PA_OK : fail_cuda(e);

@@ -29,6 +29,7 @@
 //    combines all partials and writes the output (split-context reduce in the
 //    same launch, no second kernel).
 //  * No tensor cores: single-query decode is a bandwidth-bound GEMV.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
 #include <stdint.h>
@@ -113,29 +114,62 @@ __device__ __forceinline__ float2 h2f(uint32_t bits) {
     return __half22float2(h);
 }
 
+// The 16-bit element types of q, the caches and the output.
+struct F16 {
+    static constexpr bool kBf16 = false;
+    __device__ static __forceinline__ float2 pair(uint32_t bits) { return h2f(bits); }
+    __device__ static __forceinline__ uint16_t round(float x) {
+        const __half h = __float2half_rn(x);
+        return *reinterpret_cast<const uint16_t *>(&h);
+    }
+};
+struct BF16 {
+    static constexpr bool kBf16 = true;
+    // bf16 is the top half of an fp32: widening is a shift
+    __device__ static __forceinline__ float2 pair(uint32_t bits) {
+        return make_float2(__uint_as_float(bits << 16), __uint_as_float(bits & 0xffff0000u));
+    }
+    __device__ static __forceinline__ uint16_t round(float x) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(x);
+        return *reinterpret_cast<const uint16_t *>(&b);
+    }
+};
+
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
 // Partial q.k over this lane's 8 dims of one K row (16 bytes).
+template <typename E>
 __device__ __forceinline__ float dot8(const uint4 kv, const uint4 qh, const float (&qf)[8]) {
 #if PA_DECODE_MIXED_FMA
-    // fp16 x fp16 products are exact in fp32, so fusing the conversion into
-    // the FMA gives the same result as converting first.
+    // A product of two 16-bit floats is exact in fp32, so fusing the
+    // conversion into the FMA gives the same result as converting first.
     float dot = 0.f;
     const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
     const uint32_t qw[4] = {qh.x, qh.y, qh.z, qh.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
-            "mov.b32 {a0, a1}, %1;\n\t"
-            "mov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
-            "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
-            : "+f"(dot)
-            : "r"(kw[i]), "r"(qw[i]));
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (E::kBf16) {
+            asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+                "mov.b32 {a0, a1}, %1;\n\t"
+                "mov.b32 {b0, b1}, %2;\n\t"
+                "fma.rn.f32.bf16 %0, a0, b0, %0;\n\t"
+                "fma.rn.f32.bf16 %0, a1, b1, %0;\n\t}"
+                : "+f"(dot)
+                : "r"(kw[i]), "r"(qw[i]));
+        } else {
+            asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+                "mov.b32 {a0, a1}, %1;\n\t"
+                "mov.b32 {b0, b1}, %2;\n\t"
+                "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+                "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+                : "+f"(dot)
+                : "r"(kw[i]), "r"(qw[i]));
+        }
+    }
     return dot;
 #else
     (void)qh;
-    const float2 k0 = h2f(kv.x), k1 = h2f(kv.y), k2 = h2f(kv.z), k3 = h2f(kv.w);
+    const float2 k0 = E::pair(kv.x), k1 = E::pair(kv.y), k2 = E::pair(kv.z), k3 = E::pair(kv.w);
     float dot = qf[0] * k0.x;
     dot = fmaf(qf[1], k0.y, dot);
     dot = fmaf(qf[2], k1.x, dot);
@@ -149,7 +183,7 @@ __device__ __forceinline__ float dot8(const uint4 kv, const uint4 qh, const floa
 }
 
 // One KV tile of one unit, processed by one warp.
-template <int D, int B>
+template <typename E, int D, int B>
 __device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t *vtile,
                                              const uint4 qh, const float (&qf)[8],
                                              float scale_log2, int nvalid, float &run_max,
@@ -163,7 +197,7 @@ __device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t
     float sc[C::RG];
     const uint4 *K4 = reinterpret_cast<const uint4 *>(ktile);
 #pragma unroll
-    for (int r = 0; r < C::RG; ++r) sc[r] = dot8(K4[(r * C::TPR + tr) * C::LPT + c], qh, qf);
+    for (int r = 0; r < C::RG; ++r) sc[r] = dot8<E>(K4[(r * C::TPR + tr) * C::LPT + c], qh, qf);
 
     // Reduce-scatter across the LPT lanes of a token.  Each halving step swaps
     // half of a lane's remaining partial sums with the lane `o` apart and adds
@@ -235,19 +269,20 @@ __device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t
         const float p = probs[t];
         const uint8_t *src = vrow + t * D * 2;
         if constexpr (C::DPL == 2) {
-            const float2 v = h2f(*reinterpret_cast<const uint32_t *>(src));
+            const float2 v = E::pair(*reinterpret_cast<const uint32_t *>(src));
             acc[0] = fmaf(p, v.x, acc[0]);
             acc[1] = fmaf(p, v.y, acc[1]);
         } else if constexpr (C::DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2 *>(src);
-            const float2 v0 = h2f(raw.x), v1 = h2f(raw.y);
+            const float2 v0 = E::pair(raw.x), v1 = E::pair(raw.y);
             acc[0] = fmaf(p, v0.x, acc[0]);
             acc[1] = fmaf(p, v0.y, acc[1]);
             acc[2] = fmaf(p, v1.x, acc[2]);
             acc[3] = fmaf(p, v1.y, acc[3]);
         } else {
             const uint4 raw = *reinterpret_cast<const uint4 *>(src);
-            const float2 v0 = h2f(raw.x), v1 = h2f(raw.y), v2 = h2f(raw.z), v3 = h2f(raw.w);
+            const float2 v0 = E::pair(raw.x), v1 = E::pair(raw.y), v2 = E::pair(raw.z),
+                         v3 = E::pair(raw.w);
             acc[0] = fmaf(p, v0.x, acc[0]);
             acc[1] = fmaf(p, v0.y, acc[1]);
             acc[2] = fmaf(p, v1.x, acc[2]);
@@ -271,11 +306,11 @@ __device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t
     __syncwarp();  // probs is rewritten by the next tile
 }
 
-template <int DPL>
-__device__ __forceinline__ void store_out_f16(uint16_t *dst, const float (&v)[DPL], float inv) {
-    __half h[DPL];
+template <typename E, int DPL>
+__device__ __forceinline__ void store_out(uint16_t *dst, const float (&v)[DPL], float inv) {
+    uint16_t h[DPL];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) h[i] = __float2half_rn(v[i] * inv);
+    for (int i = 0; i < DPL; ++i) h[i] = E::round(v[i] * inv);
     if constexpr (DPL == 2) {
         *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(h);
     } else if constexpr (DPL == 4) {
@@ -303,7 +338,7 @@ __device__ __forceinline__ void store_f32(float *dst, const float (&v)[DPL]) {
         *reinterpret_cast<float2 *>(dst + i) = make_float2(v[i], v[i + 1]);
 }
 
-template <int D, int B>
+template <typename E, int D, int B>
 __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     decode_kernel(const DecodeArgs a) {
     using C = Cfg<D, B>;
@@ -502,7 +537,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         const uint4 qraw =
             *reinterpret_cast<const uint4 *>(desc_q + slot * D + (lane % C::LPT) * 8);
         {
-            const float2 q0 = h2f(qraw.x), q1 = h2f(qraw.y), q2 = h2f(qraw.z), q3 = h2f(qraw.w);
+            const float2 q0 = E::pair(qraw.x), q1 = E::pair(qraw.y), q2 = E::pair(qraw.z),
+                         q3 = E::pair(qraw.w);
             qf[0] = q0.x; qf[1] = q0.y; qf[2] = q1.x; qf[3] = q1.y;
             qf[4] = q2.x; qf[5] = q2.y; qf[6] = q3.x; qf[7] = q3.y;
         }
@@ -521,7 +557,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                 const int tok0 = (p * TPU + j) * B;
                 const int nvalid = min(B, ctx - tok0);
                 const uint8_t *ktile = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
-                consume_tile<D, B>(ktile, ktile + C::TILE_BYTES, qraw, qf, a.scale_log2, nvalid,
+                consume_tile<E, D, B>(ktile, ktile + C::TILE_BYTES, qraw, qf, a.scale_log2, nvalid,
                                    run_max, run_sum, acc, probs, lane);
             }
             __syncwarp();
@@ -559,7 +595,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
             }
             const size_t sh = static_cast<size_t>(s) * H + h;
             if (np == 1) {
-                store_out_f16<C::DPL>(a.out + sh * D + lane * C::DPL, o, L > 0.f ? 1.f / L : 0.f);
+                store_out<E, C::DPL>(a.out + sh * D + lane * C::DPL, o, L > 0.f ? 1.f / L : 0.f);
             } else {
                 const size_t pidx = sh * a.max_parts + p;
                 if (lane == 0) reinterpret_cast<float2 *>(a.part_ml)[pidx] = make_float2(M, L);
@@ -593,7 +629,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
 #pragma unroll
                         for (int e = 0; e < C::DPL; ++e) go[e] = fmaf(f, v[e], go[e]);
                     }
-                    store_out_f16<C::DPL>(a.out + sh * D + lane * C::DPL, go,
+                    store_out<E, C::DPL>(a.out + sh * D + lane * C::DPL, go,
                                           GL > 0.f ? 1.f / GL : 0.f);
                     if (lane == 0) atomicExch(&a.counters[2 + sh], 0u);  // ready for the next call
                 }
@@ -606,26 +642,46 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
 }
 
 struct Variant {
-    int head_dim, block_size;
+    int dtype, head_dim, block_size;
     const void *kernel;
     int threads;
     size_t (*smem_bytes)(int);
 };
 
-template <int D, int B>
+template <typename E, int D, int B>
 Variant make_variant() {
-    return Variant{D, B, reinterpret_cast<const void *>(&decode_kernel<D, B>), Cfg<D, B>::THREADS,
+    return Variant{E::kBf16 ? PA_DTYPE_BF16 : PA_DTYPE_F16, D, B,
+                   reinterpret_cast<const void *>(&decode_kernel<E, D, B>), Cfg<D, B>::THREADS,
                    &Cfg<D, B>::smem_bytes};
 }
 
-const Variant *find_variant(int head_dim, int block_size) {
-    static const Variant variants[] = {
-        make_variant<64, 8>(),  make_variant<64, 16>(),  make_variant<64, 32>(),
-        make_variant<128, 8>(), make_variant<128, 16>(), make_variant<128, 32>(),
-        make_variant<256, 8>(), make_variant<256, 16>(), make_variant<256, 32>(),
-    };
-    for (const Variant &v : variants)
-        if (v.head_dim == head_dim && v.block_size == block_size) return &v;
+template <typename E>
+void add_variants(Variant *v) {
+    v[0] = make_variant<E, 64, 8>();   v[1] = make_variant<E, 64, 16>();
+    v[2] = make_variant<E, 64, 32>();  v[3] = make_variant<E, 128, 8>();
+    v[4] = make_variant<E, 128, 16>(); v[5] = make_variant<E, 128, 32>();
+    v[6] = make_variant<E, 256, 8>();  v[7] = make_variant<E, 256, 16>();
+    v[8] = make_variant<E, 256, 32>();
+}
+
+constexpr int kNumVariants = 18;
+
+const Variant *variants() {
+    static Variant table[kNumVariants];
+    static bool filled = [] {
+        add_variants<F16>(table);
+        add_variants<BF16>(table + 9);
+        return true;
+    }();
+    (void)filled;
+    return table;
+}
+
+const Variant *find_variant(int dtype, int head_dim, int block_size) {
+    const Variant *t = variants();
+    for (int i = 0; i < kNumVariants; ++i)
+        if (t[i].dtype == dtype && t[i].head_dim == head_dim && t[i].block_size == block_size)
+            return &t[i];
     return nullptr;
 }
 
@@ -636,8 +692,8 @@ int g_max_dynamic_smem[kMaxDevices] = {0};
 
 }  // namespace
 
-bool decode_variant_supported(int head_dim, int block_size) {
-    return find_variant(head_dim, block_size) != nullptr;
+bool decode_variant_supported(int dtype, int head_dim, int block_size) {
+    return find_variant(dtype, head_dim, block_size) != nullptr;
 }
 
 cudaError_t prepare_decode_kernels(int device) {
@@ -645,21 +701,18 @@ cudaError_t prepare_decode_kernels(int device) {
     int optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return e;
-    static const int dims[] = {64, 128, 256};
-    static const int blocks[] = {8, 16, 32};
-    for (int d : dims)
-        for (int b : blocks) {
-            const Variant *v = find_variant(d, b);
-            e = cudaFuncSetAttribute(v->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-            if (e != cudaSuccess) return e;
-        }
+    const Variant *t = variants();
+    for (int i = 0; i < kNumVariants; ++i) {
+        e = cudaFuncSetAttribute(t[i].kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (e != cudaSuccess) return e;
+    }
     g_max_dynamic_smem[device] = optin;
     return cudaSuccess;
 }
 
-cudaError_t launch_decode(const DecodeArgs &args, int head_dim, int block_size, int num_sms,
-                          cudaStream_t stream) {
-    const Variant *v = find_variant(head_dim, block_size);
+cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int block_size,
+                          int num_sms, cudaStream_t stream) {
+    const Variant *v = find_variant(dtype, head_dim, block_size);
     if (!v) return cudaErrorInvalidValue;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);

@@ -11,10 +11,10 @@ namespace pa {
 
 // Arguments of one decode launch (device pointers unless noted).
 struct DecodeArgs {
-    uint16_t *out;                 // fp16 [S, H, D]
-    const uint16_t *q;             // fp16 [S, H, D]
-    const uint16_t *k_cache;       // fp16 [N, H, B, D]
-    const uint16_t *v_cache;       // fp16 [N, H, B, D]
+    uint16_t *out;                 // fp16 or bf16 [S, H, D]
+    const uint16_t *q;             // [S, H, D]
+    const uint16_t *k_cache;       // [N, H, B, D]
+    const uint16_t *v_cache;       // [N, H, B, D]
     const int32_t *block_tables;   // [S, max_blocks_per_seq]
     const int32_t *context_lens;   // [S]
     float scale_log2;              // softmax scale * log2(e)
@@ -50,9 +50,9 @@ int record_cuda_error(cudaError_t e);
 
 // Kernel launchers (pa_decode.cu / pa_cache.cu).  They return a cudaError_t.
 // `num_sms` sizes the persistent decode grid.
-cudaError_t launch_decode(const DecodeArgs &args, int head_dim, int block_size, int num_sms,
-                          cudaStream_t stream);
-bool decode_variant_supported(int head_dim, int block_size);
+cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int block_size,
+                          int num_sms, cudaStream_t stream);
+bool decode_variant_supported(int dtype, int head_dim, int block_size);
 cudaError_t prepare_decode_kernels(int device);
 
 cudaError_t launch_reshape_and_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,

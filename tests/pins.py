@@ -126,6 +126,34 @@ def pin_half_decoding(lib):
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan])), "signed zero"
 
 
+def bf16_bits_to_float64(bits):
+    """Independent bf16 decoding through torch's own bfloat16 type."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).astype(np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def pin_bf16_decoding(lib):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bf16_bits_to_float64(bits)
+    got = np.array([oracle.bf16_to_double(int(b), lib=lib) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan), "bf16 NaN patterns differ"
+    assert np.array_equal(got[~nan], ref[~nan]), "bf16 decoding differs from torch"
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan])), "bf16 signed zero"
+
+
+def pin_brute_force_bf16(lib):
+    """bf16 inputs: brute force over values decoded by torch, not the oracle."""
+    case = workloads.build_case("bf16", [1, 16, 17, 40], num_heads=2, head_dim=8, seed=14,
+                                spare_frac=0.5, dtype="bf16")
+    got = _decode(lib, case, dtype="bf16")
+    f = lambda a: bf16_bits_to_float64(a)
+    ref = brute_force(f(case.q), f(case.k_cache), f(case.v_cache), case.block_tables,
+                      case.context_lens, case.scale)
+    assert_close(got, ref, 1e-12, "bf16 brute force")
+
+
 def pin_brute_force_tiny(lib):
     for seed, D, B, lens in ((11, 8, 16, (1, 16, 17, 40)), (12, 4, 4, (3, 9)),
                              (13, 8, 8, (40, 2))):
@@ -320,7 +348,9 @@ def pin_reshape_and_cache(lib):
 
 PINS = [
     ("half_decoding", pin_half_decoding),
+    ("bf16_decoding", pin_bf16_decoding),
     ("brute_force_tiny", pin_brute_force_tiny),
+    ("brute_force_bf16", pin_brute_force_bf16),
     ("library_attention", pin_library_attention),
     ("placement_invariance", pin_placement_invariance),
     ("shared_vs_duplicated", pin_shared_vs_duplicated),

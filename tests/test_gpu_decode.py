@@ -257,3 +257,50 @@ def test_back_to_back_steps_keep_their_order(dev):
     assert pa.device_errors() == 0
     for i, out in enumerate(outs):
         assert_parity(out.cpu().numpy(), refs[i % 2], f"step {i}")
+
+
+# ----------------------------------------------------------------------------
+# bfloat16 caches (bf16 tolerance derived in gpu_helpers)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("partition_tokens", [0, 16, 272, 1 << 16])
+def test_bf16_edge_lengths(dev, partition_tokens):
+    case = _ragged("edges_bf16", EDGE_LENS, H=3, dtype="bf16")
+    got, flags, _ = run_gpu(case, dev, partition_tokens)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), f"bf16 edges P={partition_tokens}", dtype="bf16")
+    assert (got[0] == 0).all(), "an empty context must give a zero row"
+    phys = case.block_tables[1, 0]
+    assert np.array_equal(got[1], case.v_cache[phys, :, 0, :]), "ctx 1 must return V exactly"
+
+
+def test_bf16_head_dim_block_size_variants(dev):
+    for D in (64, 128, 256):
+        for B in (8, 16, 32):
+            case = _ragged(f"bf{D}_{B}", [1, B - 1, B + 1, 333, 700], H=2, D=D, B=B,
+                           seed=3 * D + B, dtype="bf16")
+            ref = oracle.decode_case(case)
+            for P in (0, 2 * B):
+                got, flags, _ = run_gpu(case, dev, P)
+                assert flags == 0
+                assert_parity(got, ref, f"bf16 D={D} B={B} P={P}", dtype="bf16")
+
+
+def test_bf16_reshape_and_cache_bit_exact(dev):
+    import paged_kv_cache_269_gb300 as pa
+    from gpu_helpers import to_numpy
+    case = _ragged("rc_bf16", [5, 16, 17, 200], H=4, new_tokens=True, dtype="bf16")
+    d = upload(case, dev)
+    pa.reshape_and_cache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    assert pa.device_errors() == 0
+    ref_k, ref_v = oracle.reshape_and_cache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                            case.slot_mapping)
+    assert np.array_equal(to_numpy(d["k_cache"], case), ref_k)
+    assert np.array_equal(to_numpy(d["v_cache"], case), ref_v)
+
+
+def test_bf16_llama7b_full_size(dev):
+    case = workloads.make_workload("llama7b_b64", dtype="bf16")
+    got, flags, _ = run_gpu(case, dev)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), "bf16 llama7b_b64", dtype="bf16")

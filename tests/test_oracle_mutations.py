@@ -22,10 +22,13 @@ MUTATIONS = {
     "offset_shift": ("int offset = t % block_size;", "int offset = (t + 1) % block_size;"),
     "logical_block": ("max_blocks_per_seq + t / block_size];",
                       "max_blocks_per_seq + (t / block_size) / 2];"),
-    "k_from_v": ("K[(size_t)t * head_dim + d] = oracle_half_to_double(k_cache[at]);",
-                 "K[(size_t)t * head_dim + d] = oracle_half_to_double(v_cache[at]);"),
-    "q_wrong_head": ("qd[d] = oracle_half_to_double(q[(size_t)pair * head_dim + d]);",
-                     "qd[d] = oracle_half_to_double(q[(size_t)s * head_dim + d]);"),
+    "k_from_v": ("K[(size_t)t * head_dim + d] = element_to_double(k_cache[at], dtype);",
+                 "K[(size_t)t * head_dim + d] = element_to_double(v_cache[at], dtype);"),
+    "q_wrong_head": ("qd[d] = element_to_double(q[(size_t)pair * head_dim + d], dtype);",
+                     "qd[d] = element_to_double(q[(size_t)s * head_dim + d], dtype);"),
+    "bf16_shift": ("uint32_t word = (uint32_t)bits << 16;", "uint32_t word = (uint32_t)bits << 15;"),
+    "bf16_read_as_f16": ("return dtype == ORACLE_BF16 ? oracle_bf16_to_double(bits) : oracle_half_to_double(bits);",
+                         "return oracle_half_to_double(bits);"),
     "head_offset_transposed": ("size_t at = cache_index(phys, h, offset, d,",
                                "size_t at = cache_index(phys, offset % num_heads, h % block_size, d,"),
     "drop_last_token": ("weights[t] = exp(weights[t] - max_score);\n            total += weights[t];",

@@ -39,6 +39,10 @@ BLOCK_SIZE = 16
 # on all host cores while the values stay independent of the thread count.
 _CHUNK = 1 << 22
 F16_NAN = np.float16(np.nan)
+BF16_NAN_BITS = np.uint16(0x7FC0)  # a quiet NaN in bfloat16
+# Storage dtype per element type: fp16 arrays are numpy float16; bf16 arrays
+# are uint16 arrays holding the bfloat16 bit patterns (numpy has no bfloat16).
+STORAGE = {"f16": np.float16, "bf16": np.uint16}
 
 
 class OutOfBlocks(RuntimeError):
@@ -72,6 +76,7 @@ class DecodeCase:
     slot_mapping: Optional[np.ndarray] = None
     shared_prefix_blocks: int = 0
     meta: dict = field(default_factory=dict)
+    dtype: str = "f16"
 
     @property
     def num_seqs(self) -> int:
@@ -102,8 +107,15 @@ def _threads() -> int:
     return max(1, min(32, os.cpu_count() or 1))
 
 
-def fill_normal_f16(out: np.ndarray, seed: int, stream: int) -> None:
-    """Fill a contiguous fp16 array with seeded N(0, 1) draws, rounded to fp16.
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns of finite float32 values, rounded to nearest even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+
+
+def fill_normal(out: np.ndarray, seed: int, stream: int) -> None:
+    """Fill a contiguous fp16 array (or a uint16 array of bf16 bits) with
+    seeded N(0, 1) draws rounded to the element type.
 
     Chunk i of stream `stream` uses Philox seeded by SeedSequence(seed,
     spawn_key=(stream,)).spawn(...)[i], so the values do not depend on how many
@@ -120,13 +132,20 @@ def fill_normal_f16(out: np.ndarray, seed: int, stream: int) -> None:
         lo = i * _CHUNK
         hi = min(n, lo + _CHUNK)
         g = np.random.Generator(np.random.Philox(children[i]))
-        flat[lo:hi] = g.standard_normal(hi - lo, dtype=np.float32)
+        draws = g.standard_normal(hi - lo, dtype=np.float32)
+        if flat.dtype == np.uint16:
+            flat[lo:hi] = f32_to_bf16_bits(draws)
+        else:
+            flat[lo:hi] = draws
 
     if nchunks == 1:
         work(0)
     else:
         with ThreadPoolExecutor(_threads()) as ex:
             list(ex.map(work, range(nchunks)))
+
+
+fill_normal_f16 = fill_normal  # the name used before bf16 support
 
 
 # ----------------------------------------------------------------------------
@@ -179,8 +198,9 @@ def poison_unused(case: DecodeCase) -> None:
             n = min(B, ctx - b * B)
             covered[phys, :n] = True
     blk, off = np.nonzero(~covered)
+    nan = BF16_NAN_BITS if case.dtype == "bf16" else F16_NAN
     for cache in (case.k_cache, case.v_cache):
-        cache[blk, :, off, :] = F16_NAN
+        cache[blk, :, off, :] = nan
 
 
 # ----------------------------------------------------------------------------
@@ -192,7 +212,7 @@ def build_case(name: str, context_lens, *, num_heads: int, head_dim: int,
                num_blocks: Optional[int] = None, spare_frac: float = 0.10,
                max_blocks_per_seq: Optional[int] = None,
                shared_prefix_blocks: int = 0, new_tokens: bool = False,
-               poison: bool = True, values: bool = True) -> DecodeCase:
+               poison: bool = True, values: bool = True, dtype: str = "f16") -> DecodeCase:
     """Generic builder; the named workloads below are thin wrappers.
 
     The pool holds exactly the blocks the tables use plus `spare_frac` spare
@@ -215,8 +235,9 @@ def build_case(name: str, context_lens, *, num_heads: int, head_dim: int,
     tables = allocate_tables(ctx, block_size, num_blocks, max_blocks_per_seq, rng,
                              shared_prefix_blocks)
     H, D = num_heads, head_dim
-    q = np.empty((S, H, D), dtype=np.float16)
-    k_cache = np.empty((num_blocks, H, block_size, D), dtype=np.float16)
+    st = STORAGE[dtype]
+    q = np.empty((S, H, D), dtype=st)
+    k_cache = np.empty((num_blocks, H, block_size, D), dtype=st)
     v_cache = np.empty_like(k_cache)
     if values:
         fill_normal_f16(q, seed, 1)
@@ -227,7 +248,7 @@ def build_case(name: str, context_lens, *, num_heads: int, head_dim: int,
                       scale=float(np.float32(1.0 / math.sqrt(D))),
                       context_lens=ctx, block_tables=tables, q=q,
                       k_cache=k_cache, v_cache=v_cache,
-                      shared_prefix_blocks=shared_prefix_blocks)
+                      shared_prefix_blocks=shared_prefix_blocks, dtype=dtype)
     if poison and values:
         poison_unused(case)
     if new_tokens:
@@ -252,7 +273,7 @@ def add_new_tokens(case: DecodeCase) -> None:
         slots.append(int(case.block_tables[s, pos // B]) * B + pos % B)
     T = len(slots)
     case.slot_mapping = np.asarray(slots, dtype=np.int32)
-    case.k_new = np.empty((T, case.num_heads, case.head_dim), dtype=np.float16)
+    case.k_new = np.empty((T, case.num_heads, case.head_dim), dtype=case.q.dtype)
     case.v_new = np.empty_like(case.k_new)
     fill_normal_f16(case.k_new, case.seed, 4)
     fill_normal_f16(case.v_new, case.seed, 5)

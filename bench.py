@@ -47,8 +47,13 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--op", choices=["step", "copy_blocks", "swap_out", "swap_in"], default="step",
+                   help="step: reshape_and_cache + decode (the hot path); the others time "
+                        "pa_copy_blocks on a 4096-block pool, 2048 random pairs")
     p.add_argument("--workload", default="llama7b_b64", choices=workloads.WORKLOADS)
     p.add_argument("--partition-tokens", type=int, default=0)
+    p.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
+                   help="element type of q, the caches and the output")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU work the oracle baseline leg runs for (bounded sample)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -187,7 +192,8 @@ def oracle_sample(case, seconds):
         if case.num_new_tokens:
             kc, vc = oracle.reshape_and_cache(case.k_new, case.v_new, case.k_cache, case.v_cache,
                                               case.slot_mapping, lib=lib)
-        oracle.decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale, lib=lib)
+        oracle.decode(case.q, kc, vc, case.block_tables, case.context_lens, case.scale, lib=lib,
+                      dtype=case.dtype)
         runs += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -198,7 +204,7 @@ def oracle_sample(case, seconds):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    case = workloads.make_workload(args.workload)
+    case = workloads.make_workload(args.workload, dtype=args.dtype)
     nbytes = step_bytes(case)
     # each step: one full pass of the oracle over the workload
     per_step, cores = [], 0
@@ -248,16 +254,23 @@ def run_native(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     pa.lib()
-    case = workloads.make_workload(args.workload, new_tokens=True)
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    case = workloads.make_workload(args.workload, new_tokens=True, dtype=args.dtype)
+    et = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+
+    def t(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:  # bf16 bit patterns
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
     d = dict(q=t(case.q), k_cache=t(case.k_cache), v_cache=t(case.v_cache),
              block_tables=t(case.block_tables), context_lens=t(case.context_lens),
              k_new=t(case.k_new), v_new=t(case.v_new), slot_mapping=t(case.slot_mapping))
-    out = torch.empty(case.q.shape, dtype=torch.float16, device=dev)
+    out = torch.empty(case.q.shape, dtype=et, device=dev)
     stream = torch.cuda.Stream(dev)
     nws = pa.decode_workspace_bytes(case.num_seqs, case.num_heads, case.head_dim,
                                     case.block_size, case.num_blocks, case.max_blocks_per_seq,
-                                    args.partition_tokens)
+                                    args.partition_tokens, dtype=1 if args.dtype == "bf16" else 0)
     ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
     ctr = torch.zeros(pa.decode_counters_bytes(case.num_seqs, case.num_heads) // 4,
                       dtype=torch.int32, device=dev)
@@ -338,7 +351,8 @@ def run_native(args, rank, world, local_rank):
         for k in names:
             hb[offsets[k]:offsets[k] + arrays[k].nbytes] = arrays[k].view(np.uint8).reshape(-1)
         dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-        tdt = {np.dtype(np.float16): torch.float16, np.dtype(np.int32): torch.int32}
+        tdt = {np.dtype(np.float16): torch.float16, np.dtype(np.int32): torch.int32,
+               np.dtype(np.uint16): torch.bfloat16}
         dev_in = {k: dev_buf[offsets[k]:offsets[k] + arrays[k].nbytes].view(
             tdt[arrays[k].dtype]).view(arrays[k].shape) for k in names}
         out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -391,7 +405,7 @@ def run_native(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
         "data": "synthetic", "config": config_of(case, args),
         "tokens_per_s": round(world * case.num_seqs / (step_ms * 1e-3), 1),
         "pct_of_peak": round(100 * value / peak, 2),
@@ -413,6 +427,83 @@ def run_native(args, rank, world, local_rank):
     print(json.dumps(line))
 
 
+def run_copy_op(args, local_rank):
+    """Time pa_copy_blocks: device -> device (copy-on-write), device -> pinned
+    host (swap out) or pinned host -> device (swap in)."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    N, H, B, D, n = 4096, 32, 16, 128, 2048
+    g = torch.Generator(device=dev).manual_seed(11)
+    kc = torch.randn((N, H, B, D), generator=g, device=dev).half()
+    vc = torch.randn((N, H, B, D), generator=g, device=dev).half()
+    src = torch.randperm(N, device=dev, generator=g)[:n]
+    block_bytes = H * B * D * 2
+    if args.op == "copy_blocks":
+        dk, dv = torch.empty_like(kc), torch.empty_like(vc)
+        pairs = torch.stack([src, torch.randperm(N, device=dev, generator=g)[:n]], 1)
+        a_k, a_v, b_k, b_v = kc, vc, dk, dv
+    elif args.op == "swap_out":
+        b_k = torch.empty((n, H, B, D), dtype=torch.float16).pin_memory()
+        b_v = torch.empty_like(b_k).pin_memory()
+        pairs = torch.stack([src, torch.arange(n, device=dev)], 1)
+        a_k, a_v = kc, vc
+    else:  # swap_in
+        a_k = torch.randn((n, H, B, D)).half().pin_memory()
+        a_v = torch.randn((n, H, B, D)).half().pin_memory()
+        pairs = torch.stack([torch.arange(n, device=dev), src], 1)
+        b_k, b_v = kc, vc
+    pairs = pairs.to(torch.int32).contiguous()
+    stream = torch.cuda.Stream(dev)
+    call = lambda: pa.copy_blocks(a_k, a_v, b_k, b_v, pairs, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize(dev)
+    assert pa.device_errors(stream=stream) == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    moved = 2 * n * block_bytes                   # K and V, one direction
+    if args.op == "copy_blocks":
+        alg, peak, src_note = 2 * moved, measured_peaks()[0], "MEASURED_PEAKS.json hbm_gbs"
+    else:
+        # the link ceiling measured here: one contiguous cudaMemcpyAsync of
+        # the same byte count in the same direction
+        host = torch.empty(moved // 2, dtype=torch.float16).pin_memory()
+        devbuf = torch.empty(moved // 2, dtype=torch.float16, device=dev)
+        cp = (lambda: host.copy_(devbuf, non_blocking=True)) if args.op == "swap_out" else \
+             (lambda: devbuf.copy_(host, non_blocking=True))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                cp()
+            e0.record(stream)
+            for _ in range(args.steps):
+                cp()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        alg = moved
+        peak = moved / (e0.elapsed_time(e1) / args.steps * 1e-3) / 1e9
+        src_note = "contiguous cudaMemcpyAsync of the same bytes, measured in this run"
+    achieved = alg / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": f"pa_copy_blocks {args.op} GB/s", "value": round(achieved, 2), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"op": args.op, "pool_blocks": N, "pairs": n, "num_heads": H, "block_size": B,
+                   "head_dim": D, "block_bytes_k_plus_v": 2 * block_bytes},
+        "roofline": {"bound": "hbm" if args.op == "copy_blocks" else "host link",
+                     "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": src_note,
+                     "algorithmic_bytes_per_launch": int(alg)},
+        "gpu_launches": args.steps}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -420,6 +511,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.op != "step":
+        if rank == 0:
+            run_copy_op(args, local_rank)
         return
     if world > 1:
         import torch

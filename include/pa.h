@@ -108,6 +108,38 @@ int pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_ca
                          const pa_dims *dims, void *stream);
 
 /*
+ * pa_copy_blocks -- copy whole KV blocks between two block pools.
+ *
+ * Source: the KV cache manager's block moves -- blocks shared between
+ * requests through reference counts, so a request that must change a shared
+ * block gets its own copy, and blocks swapped out to CPU memory when GPU
+ * memory runs short and swapped back in later (doramagic.ai vLLM manual,
+ * "内存管理策略", "BlockPool 组件", "共享机制").  One call covers copy-on-write
+ * (source pool = destination pool), swap-out (device -> host) and swap-in
+ * (host -> device).
+ *
+ *   src_k, src_v    [src_num_blocks, H, B, D] 16-bit elements: the source pool
+ *   dst_k, dst_v    [dst_num_blocks, H, B, D]: the destination pool (written)
+ *   block_pairs     device (or device-addressable), int32 [num_pairs][2]:
+ *                   (source block, destination block)
+ *   num_pairs       >= 0 (0 launches nothing)
+ *   dims            host; num_heads, head_dim, block_size and dtype are used
+ *   stream          cudaStream_t
+ *
+ * Every pool pointer must be memory the current device can address in a
+ * kernel: its own device memory, managed memory, pinned or registered host
+ * memory (cudaHostAlloc / cudaHostRegister), or any host memory when the
+ * device reports cudaDevAttrPageableMemoryAccess.  Anything else returns
+ * PA_ERR_UNSUPPORTED before launching.  For each pair, K and V of block src
+ * (all heads) are copied bit for bit to block dst.  A pair with an id outside
+ * its pool is skipped and sets PA_DEVERR_TABLE.  Destinations must be
+ * distinct and must not be the source of another pair (such copies race).
+ */
+int pa_copy_blocks(const void *src_k, const void *src_v, int32_t src_num_blocks, void *dst_k,
+                   void *dst_v, int32_t dst_num_blocks, const int32_t *block_pairs,
+                   int32_t num_pairs, const pa_dims *dims, void *stream);
+
+/*
  * pa_decode -- paged-attention decode for a batch of sequences.
  *
  * Source: o = Attention(q_t, K_{1:t}, V_{1:t}) ("vLLM 2026 推理引擎全解",

@@ -66,6 +66,8 @@ def load(path: str = _LIB_PATH, src: str = _SRC):
     lib.oracle_reshape_and_cache.argtypes = [u16p, u16p, u16p, u16p, i32p,
                                              ci, ci, ci, ci, ci]
     lib.oracle_reshape_and_cache.restype = ci
+    lib.oracle_copy_blocks.argtypes = [u16p, u16p, ci, u16p, u16p, ci, i32p, ci, ci, ci, ci]
+    lib.oracle_copy_blocks.restype = ci
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_half_to_double.restype = ctypes.c_double
     lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -146,6 +148,24 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, lib=None):
     if rc != 0:
         raise OracleError(ERRORS.get(rc, str(rc)))
     return kc, vc
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs, lib=None):
+    """Return updated copies of (dst_k, dst_v) with K/V of block src copied to
+    block dst for every row (src, dst) of block_pairs [n, 2]."""
+    lib = lib or _get()
+    Ns, H, B, D = src_k.shape
+    Nd = dst_k.shape[0]
+    if src_v.shape != src_k.shape or dst_v.shape != dst_k.shape or dst_k.shape[1:] != (H, B, D):
+        raise OracleError("shape mismatch")
+    dk = np.array(dst_k, copy=True, order="C")
+    dv = np.array(dst_v, copy=True, order="C")
+    sk, sv, pp = _u16(src_k), _u16(src_v), _i32(np.asarray(block_pairs).reshape(-1, 2))
+    dku, dvu = _u16(dk), _u16(dv)
+    rc = lib.oracle_copy_blocks(sk[1], sv[1], Ns, dku[1], dvu[1], Nd, pp[1], pp[0].shape[0], H, D, B)
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, str(rc)))
+    return dk, dv
 
 
 def decode_case(case, lib=None) -> np.ndarray:

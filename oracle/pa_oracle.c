@@ -253,3 +253,39 @@ int oracle_reshape_and_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_c
     }
     return ORACLE_OK;
 }
+
+/*
+ * copy_blocks: for each pair (src, dst) of block_pairs [num_pairs][2], copy K
+ * and V of block src of the source pool, every head, to block dst of the
+ * destination pool -- the KV cache manager's block copy and CPU swap
+ * (doramagic.ai vLLM manual, "内存管理策略", "BlockPool 组件").
+ *
+ * Pools are [num_blocks, num_heads, block_size, head_dim] 16-bit elements.
+ * Returns ORACLE_BAD_TABLE, without copying anything, if an id is out of its
+ * pool.
+ */
+int oracle_copy_blocks(const uint16_t *src_k, const uint16_t *src_v, int src_num_blocks,
+                       uint16_t *dst_k, uint16_t *dst_v, int dst_num_blocks,
+                       const int32_t *block_pairs, int num_pairs, int num_heads, int head_dim,
+                       int block_size)
+{
+    if (num_pairs < 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return ORACLE_BAD_ARG;
+    for (int i = 0; i < num_pairs; ++i) {
+        int32_t src = block_pairs[2 * i], dst = block_pairs[2 * i + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks)
+            return ORACLE_BAD_TABLE;
+    }
+    for (int i = 0; i < num_pairs; ++i) {
+        int64_t src = block_pairs[2 * i], dst = block_pairs[2 * i + 1];
+        for (int h = 0; h < num_heads; ++h)
+            for (int t = 0; t < block_size; ++t)
+                for (int d = 0; d < head_dim; ++d) {
+                    size_t from = cache_index(src, h, t, d, num_heads, block_size, head_dim);
+                    size_t to = cache_index(dst, h, t, d, num_heads, block_size, head_dim);
+                    dst_k[to] = src_k[from];
+                    dst_v[to] = src_v[from];
+                }
+    }
+    return ORACLE_OK;
+}

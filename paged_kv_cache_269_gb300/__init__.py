@@ -9,6 +9,7 @@ unbuildable library raises.
 
 Functions (names follow the C ABI):
   reshape_and_cache(k, v, k_cache, v_cache, slot_mapping)
+  copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs)
   decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, ...)
   decode_workspace_bytes(...), decode_counters_bytes(...), device_errors(), version()
 """
@@ -19,7 +20,7 @@ import threading
 
 from . import build as _build
 
-__all__ = ["PaError", "Dims", "lib", "reshape_and_cache", "decode", "decode_workspace_bytes",
+__all__ = ["PaError", "Dims", "lib", "reshape_and_cache", "copy_blocks", "decode", "decode_workspace_bytes",
            "decode_counters_bytes", "device_errors", "reset_workspaces", "version", "DEVERR_TABLE", "DEVERR_CONTEXT",
            "DEVERR_SLOT", "DEVERR_TIMEOUT"]
 
@@ -32,7 +33,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_UNSUPPO
           -4: "PA_ERR_ALIGN", -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_CUDA"}
 
 # Every symbol include/pa.h declares.
-EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_bytes",
+EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes",
            "pa_decode_counters_bytes", "pa_decode_ws", "pa_decode_static", "pa_device_errors",
            "pa_status_string", "pa_last_cuda_error", "pa_version")
 _SIZE_ERROR = (1 << 64) - 1
@@ -62,6 +63,7 @@ def _declare(l):
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     dp = ctypes.POINTER(Dims)
     l.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, dp, vp]
+    l.pa_copy_blocks.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, dp, vp]
     l.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp]
     l.pa_decode_workspace_bytes.argtypes = [dp, i32, i32]
     l.pa_decode_workspace_bytes.restype = sz
@@ -76,7 +78,8 @@ def _declare(l):
     l.pa_status_string.restype = ctypes.c_char_p
     l.pa_last_cuda_error.argtypes = []
     l.pa_version.argtypes = []
-    for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_ws", "pa_device_errors",
+    for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_ws",
+                 "pa_device_errors",
                  "pa_last_cuda_error", "pa_version"):
         getattr(l, name).restype = ctypes.c_int
     return l
@@ -179,6 +182,41 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None):
         rc = lib().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(slot_mapping), T, ctypes.byref(dims), sh)
     _check(rc, "pa_reshape_and_cache")
+
+
+def copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
+    """Copy K and V of block src to block dst (all heads) for every row
+    (src, dst) of block_pairs [n, 2] int32 (a CUDA tensor).  The pools are
+    [N, H, B, D] tensors of one 16-bit dtype, each on the CUDA device or in
+    pinned host memory, so one call does copy-on-write (same pool), swap-out
+    (device -> pinned host) or swap-in (pinned host -> device)."""
+    torch = _torch()
+    if not isinstance(block_pairs, torch.Tensor) or not block_pairs.is_cuda:
+        raise ValueError("block_pairs must be a CUDA tensor")
+    dev = block_pairs.device
+    if block_pairs.dtype != torch.int32 or block_pairs.dim() != 2 or block_pairs.shape[1] != 2 \
+            or not block_pairs.is_contiguous():
+        raise ValueError("block_pairs must be a contiguous int32 [n, 2] tensor")
+    _element_dtype(src_k)
+    for name, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != src_k.dtype or t.dim() != 4 \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-d tensor of {src_k.dtype}")
+        if t.is_cuda:
+            if t.device != dev:
+                raise ValueError(f"{name} is on {t.device}, expected {dev}")
+        elif not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if src_v.shape != src_k.shape or dst_v.shape != dst_k.shape or src_k.shape[1:] != dst_k.shape[1:]:
+        raise ValueError("copy_blocks: inconsistent pool shapes")
+    N_src, H, B, D = src_k.shape
+    dims = Dims(0, H, D, B, N_src, _element_dtype(src_k))
+    sh, _ = _stream_handle(dev, stream)
+    with torch.cuda.device(dev):
+        rc = lib().pa_copy_blocks(_ptr(src_k), _ptr(src_v), N_src, _ptr(dst_k), _ptr(dst_v),
+                                  dst_k.shape[0], _ptr(block_pairs), block_pairs.shape[0],
+                                  ctypes.byref(dims), sh)
+    _check(rc, "pa_copy_blocks")
 
 
 def decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, num_blocks,

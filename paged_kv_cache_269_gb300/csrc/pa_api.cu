@@ -96,6 +96,30 @@ int partition_plan(const pa_dims *dims, int32_t max_blocks_per_seq, int32_t part
     return PA_OK;
 }
 
+// PA_OK if the current device can read and write `p` in a kernel: device
+// memory of this device, managed memory, pinned or registered host memory,
+// or any host memory when the device has coherent access to pageable memory.
+int check_device_addressable(const void *p, int device) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // the failed query leaves a (non-sticky) error behind
+        return PA_ERR_UNSUPPORTED;
+    }
+    switch (attr.type) {
+        case cudaMemoryTypeDevice:
+            return attr.device == device ? PA_OK : PA_ERR_UNSUPPORTED;
+        case cudaMemoryTypeManaged:
+        case cudaMemoryTypeHost:
+            return PA_OK;
+        default: {
+            int pageable = 0;
+            e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, device);
+            return (e == cudaSuccess && pageable) ? PA_OK : PA_ERR_UNSUPPORTED;
+        }
+    }
+}
+
 }  // namespace
 
 int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
@@ -140,6 +164,40 @@ int pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_ca
         static_cast<uint16_t *>(k_cache), static_cast<uint16_t *>(v_cache), slot_mapping,
         num_tokens, dims->num_heads, dims->head_dim, dims->block_size, dims->num_blocks, st->err,
         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+int pa_copy_blocks(const void *src_k, const void *src_v, int32_t src_num_blocks, void *dst_k,
+                   void *dst_v, int32_t dst_num_blocks, const int32_t *block_pairs,
+                   int32_t num_pairs, const pa_dims *dims, void *stream) {
+    if (!dims) return PA_ERR_NULL;
+    if (dims->num_heads <= 0 || dims->head_dim <= 0 || dims->block_size <= 0 || num_pairs < 0 ||
+        src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return PA_ERR_SHAPE;
+    if (!decode_variant_supported(dims->dtype, dims->head_dim, dims->block_size))
+        return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !block_pairs) return PA_ERR_NULL;
+    if (!aligned(src_k, 16) || !aligned(src_v, 16) || !aligned(dst_k, 16) || !aligned(dst_v, 16) ||
+        !aligned(block_pairs, 4))
+        return PA_ERR_ALIGN;
+    DeviceState *st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    for (const void *p : {src_k, src_v, static_cast<const void *>(dst_k),
+                          static_cast<const void *>(dst_v),
+                          static_cast<const void *>(block_pairs)}) {
+        rc = check_device_addressable(p, dev);
+        if (rc != PA_OK) return rc;
+    }
+    e = launch_copy_blocks(static_cast<const uint16_t *>(src_k), static_cast<const uint16_t *>(src_v),
+                           static_cast<uint16_t *>(dst_k), static_cast<uint16_t *>(dst_v),
+                           block_pairs, num_pairs, dims->num_heads, dims->head_dim,
+                           dims->block_size, src_num_blocks, dst_num_blocks, st->num_sms, st->err,
+                           static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : fail_cuda(e);
 }
 

@@ -45,6 +45,12 @@ struct WorkspaceLayout {
 void workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t max_parts,
                       WorkspaceLayout *out);
 
+cudaError_t launch_copy_blocks(const uint16_t *src_k, const uint16_t *src_v, uint16_t *dst_k,
+                               uint16_t *dst_v, const int32_t *block_pairs, int32_t num_pairs,
+                               int32_t num_heads, int32_t head_dim, int32_t block_size,
+                               int32_t src_num_blocks, int32_t dst_num_blocks, int num_sms,
+                               unsigned int *err, cudaStream_t stream);
+
 // Record a CUDA error for pa_last_cuda_error() and return PA_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
 

@@ -346,6 +346,45 @@ def pin_reshape_and_cache(lib):
     assert np.array_equal(got, one.v_new.astype(np.float64))
 
 
+def pin_copy_blocks(lib):
+    """Block copy against numpy indexing; a copy-on-write of the shared prefix
+    followed by retargeting the tables leaves the attention unchanged; a swap
+    out to a second pool and back in elsewhere leaves it unchanged too."""
+    case = workloads.build_case("cow", [40, 57, 33, 48], num_heads=2, head_dim=16, seed=42,
+                                shared_prefix_blocks=2, spare_frac=2.0)
+    base = _decode(lib, case)
+    used = set(case.block_tables[case.block_tables >= 0].tolist())
+    free = [b for b in range(case.num_blocks) if b not in used]
+    # sequences 1..3 get private copies of the two prefix blocks
+    pairs, tables = [], case.block_tables.copy()
+    for s in range(1, 4):
+        for b in range(2):
+            dst = free.pop()
+            pairs.append((int(case.block_tables[s, b]), dst))
+            tables[s, b] = dst
+    pairs = np.array(pairs, np.int32)
+    kc, vc = oracle.copy_blocks(case.k_cache, case.v_cache, case.k_cache, case.v_cache, pairs, lib=lib)
+    ref_k, ref_v = case.k_cache.copy(), case.v_cache.copy()
+    ref_k[pairs[:, 1]] = case.k_cache[pairs[:, 0]]
+    ref_v[pairs[:, 1]] = case.v_cache[pairs[:, 0]]
+    assert np.array_equal(kc.view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(vc.view(np.uint16), ref_v.view(np.uint16))
+    assert np.array_equal(_decode(lib, case, k_cache=kc, v_cache=vc, block_tables=tables), base)
+    # swap out every used block to a host pool, back in at shuffled places
+    ids = np.array(sorted(used), np.int32)
+    host_k = np.zeros((len(ids),) + case.k_cache.shape[1:], case.k_cache.dtype)
+    host_v = np.zeros_like(host_k)
+    out_pairs = np.stack([ids, np.arange(len(ids), dtype=np.int32)], 1)
+    host_k, host_v = oracle.copy_blocks(case.k_cache, case.v_cache, host_k, host_v, out_pairs, lib=lib)
+    perm = np.random.default_rng(1).permutation(case.num_blocks)[:len(ids)].astype(np.int32)
+    blank_k = np.zeros_like(case.k_cache)
+    in_pairs = np.stack([np.arange(len(ids), dtype=np.int32), perm], 1)
+    k2, v2 = oracle.copy_blocks(host_k, host_v, blank_k, np.zeros_like(blank_k), in_pairs, lib=lib)
+    remap = dict(zip(ids.tolist(), perm.tolist()))
+    t2 = np.vectorize(lambda b: remap.get(int(b), -1))(case.block_tables).astype(np.int32)
+    assert np.array_equal(_decode(lib, case, k_cache=k2, v_cache=v2, block_tables=t2), base)
+
+
 PINS = [
     ("half_decoding", pin_half_decoding),
     ("bf16_decoding", pin_bf16_decoding),
@@ -362,4 +401,5 @@ PINS = [
     ("page_example", pin_page_example),
     ("masking", pin_masking),
     ("reshape_and_cache", pin_reshape_and_cache),
+    ("copy_blocks", pin_copy_blocks),
 ]

@@ -39,6 +39,8 @@ MUTATIONS = {
                        "int offset = (slot + 1) % block_size;\n        for (int h = 0; h < num_heads; ++h) {"),
     "reshape_skips_zero": ("if (slot < 0)\n            continue;", "if (slot <= 0)\n            continue;"),
     "reshape_k_only": ("v_cache[dst] = v[src];", "v_cache[dst] = k[src];"),
+    "copy_v_from_k": ("dst_v[to] = src_v[from];", "dst_v[to] = src_k[from];"),
+    "copy_wrong_head": ("size_t to = cache_index(dst, h, t, d,", "size_t to = cache_index(dst, 0, t, d,"),
 }
 
 

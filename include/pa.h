@@ -42,10 +42,12 @@ typedef enum pa_status {
     PA_OK = 0,
     PA_ERR_NULL = -1,          /* a required pointer is NULL                    */
     PA_ERR_SHAPE = -2,         /* a size is negative, zero where it must not be, or overflows */
-    PA_ERR_UNSUPPORTED = -3,   /* head_dim / block_size outside the built variants */
+    PA_ERR_UNSUPPORTED = -3,   /* head_dim / block_size / dtype outside the built variants,
+                                  or memory the device cannot address */
     PA_ERR_ALIGN = -4,         /* an fp16 pointer is not 16-byte aligned        */
     PA_ERR_WORKSPACE = -5,     /* workspace or counter buffer missing, too small or misaligned */
-    PA_ERR_CUDA = -6           /* a CUDA runtime call failed; see pa_last_cuda_error() */
+    PA_ERR_CUDA = -6,          /* a CUDA runtime call failed; see pa_last_cuda_error() */
+    PA_ERR_OUT_OF_BLOCKS = -7  /* the KV block manager's free list is empty             */
 } pa_status;
 
 /* Bits of the per-device error word (pa_device_errors). */
@@ -258,6 +260,63 @@ int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_ca
 int pa_decode_static(void *out, const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, const int32_t *context_lens, float scale,
                      int32_t max_blocks_per_seq, const pa_dims *dims, void *stream);
+
+/*
+ * KV block manager (host only; no CUDA call).
+ *
+ * The bookkeeping half of the paged cache: blocks are handed out one at a
+ * time from a free list, ceil(tokens / block_size) per sequence, and running
+ * out is an error (doramagic.ai vLLM manual, "KVCacheManager 缓存管理"); each
+ * sequence keeps a block table of logical -> physical blocks ("vLLM 2026
+ * 推理引擎全解", §2.1); blocks may be shared -- a system prompt's full blocks
+ * between requests, or every block between the samples forked from one prompt
+ * -- and are counted by reference and freed at zero ("vLLM 2026 推理引擎全解",
+ * §2.3; mjmagnets.cn vLLM tutorial, §2.1; doramagic.ai vLLM manual, "共享机制").
+ * An append that would write into a block another sequence still references
+ * first takes a fresh block and reports a (source, destination) pair to copy
+ * with pa_copy_blocks (copy-on-write).
+ *
+ * Sequence ids are small non-negative integers, reused after pa_kvm_free.
+ * Calls return a pa_status (PA_ERR_OUT_OF_BLOCKS when the free list is
+ * empty, leaving the manager unchanged) unless stated.  Not thread-safe.
+ */
+typedef struct pa_kv_manager pa_kv_manager;
+
+/* A manager of blocks 0 .. num_blocks-1.  shuffle_seed != 0 shuffles the
+ * free list with a seeded Fisher-Yates (splitmix64); 0 keeps 0, 1, 2, ...
+ * Returns NULL on invalid sizes or out of host memory. */
+pa_kv_manager *pa_kvm_create(int32_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                             uint64_t shuffle_seed);
+void pa_kvm_destroy(pa_kv_manager *m);
+/* Free blocks (-1 for a NULL manager). */
+int32_t pa_kvm_num_free_blocks(const pa_kv_manager *m);
+/* Reference count of a block (-1 if out of range). */
+int32_t pa_kvm_refcount(const pa_kv_manager *m, int32_t block);
+/* A new sequence holding num_tokens tokens.  With parent >= 0, its first
+ * shared_blocks blocks are the parent's (they must be full in the parent and
+ * lie within num_tokens); the rest are fresh.  With parent < 0,
+ * shared_blocks must be 0. */
+int pa_kvm_add_sequence(pa_kv_manager *m, int32_t num_tokens, int32_t parent,
+                        int32_t shared_blocks, int32_t *seq_out);
+/* A new sequence sharing every block of parent, a partial last one included. */
+int pa_kvm_fork(pa_kv_manager *m, int32_t parent, int32_t *seq_out);
+/* Extend seq by one token: *slot_out = its slot (block * block_size + offset).
+ * If that token lands in a block another sequence references, the block is
+ * replaced by a fresh one and *copy_src_out / *copy_dst_out name the copy to
+ * make before writing the token; otherwise both are -1. */
+int pa_kvm_append(pa_kv_manager *m, int32_t seq, int32_t *slot_out, int32_t *copy_src_out,
+                  int32_t *copy_dst_out);
+/* Release a sequence and its block references. */
+int pa_kvm_free(pa_kv_manager *m, int32_t seq);
+/* Tokens of seq (-1 if unknown). */
+int32_t pa_kvm_context_len(const pa_kv_manager *m, int32_t seq);
+/* Slot of token `token` of seq. */
+int pa_kvm_slot(const pa_kv_manager *m, int32_t seq, int32_t token, int32_t *slot_out);
+/* Batch rows: for each seqs[i] (host), row i of tables_out [num_seqs, row_len]
+ * gets the block table padded with -1 and context_lens_out[i] its length; a
+ * negative seqs[i] gives an empty row of length 0 (batch padding). */
+int pa_kvm_block_tables(const pa_kv_manager *m, const int32_t *seqs, int32_t num_seqs,
+                        int32_t *tables_out, int32_t row_len, int32_t *context_lens_out);
 
 /*
  * Wait for `stream`, then return (in *flags, host) and clear the current

@@ -20,7 +20,7 @@ import threading
 
 from . import build as _build
 
-__all__ = ["PaError", "Dims", "lib", "reshape_and_cache", "copy_blocks", "decode", "decode_workspace_bytes",
+__all__ = ["PaError", "Dims", "KVManager", "lib", "reshape_and_cache", "copy_blocks", "decode", "decode_workspace_bytes",
            "decode_counters_bytes", "device_errors", "reset_workspaces", "version", "DEVERR_TABLE", "DEVERR_CONTEXT",
            "DEVERR_SLOT", "DEVERR_TIMEOUT"]
 
@@ -30,12 +30,16 @@ DEVERR_SLOT = 0x4
 DEVERR_TIMEOUT = 0x8
 
 STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_UNSUPPORTED",
-          -4: "PA_ERR_ALIGN", -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_CUDA"}
+          -4: "PA_ERR_ALIGN", -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_CUDA",
+          -7: "PA_ERR_OUT_OF_BLOCKS"}
 
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes",
            "pa_decode_counters_bytes", "pa_decode_ws", "pa_decode_static", "pa_device_errors",
-           "pa_status_string", "pa_last_cuda_error", "pa_version")
+           "pa_status_string", "pa_last_cuda_error", "pa_version",
+           "pa_kvm_create", "pa_kvm_destroy", "pa_kvm_num_free_blocks", "pa_kvm_refcount",
+           "pa_kvm_add_sequence", "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free",
+           "pa_kvm_context_len", "pa_kvm_slot", "pa_kvm_block_tables")
 _SIZE_ERROR = (1 << 64) - 1
 
 
@@ -78,6 +82,24 @@ def _declare(l):
     l.pa_status_string.restype = ctypes.c_char_p
     l.pa_last_cuda_error.argtypes = []
     l.pa_version.argtypes = []
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    l.pa_kvm_create.argtypes = [i32, i32, i32, ctypes.c_uint64]
+    l.pa_kvm_create.restype = vp
+    l.pa_kvm_destroy.argtypes = [vp]
+    l.pa_kvm_destroy.restype = None
+    l.pa_kvm_num_free_blocks.argtypes = [vp]
+    l.pa_kvm_refcount.argtypes = [vp, i32]
+    l.pa_kvm_add_sequence.argtypes = [vp, i32, i32, i32, i32p]
+    l.pa_kvm_fork.argtypes = [vp, i32, i32p]
+    l.pa_kvm_append.argtypes = [vp, i32, i32p, i32p, i32p]
+    l.pa_kvm_free.argtypes = [vp, i32]
+    l.pa_kvm_context_len.argtypes = [vp, i32]
+    l.pa_kvm_slot.argtypes = [vp, i32, i32, i32p]
+    l.pa_kvm_block_tables.argtypes = [vp, vp, i32, vp, i32, vp]
+    for name in ("pa_kvm_num_free_blocks", "pa_kvm_refcount", "pa_kvm_add_sequence",
+                 "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free", "pa_kvm_context_len",
+                 "pa_kvm_slot", "pa_kvm_block_tables"):
+        getattr(l, name).restype = i32
     for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_ws",
                  "pa_device_errors",
                  "pa_last_cuda_error", "pa_version"):
@@ -327,6 +349,79 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                             counters.numel() * 4, sh)
     _check(rc, "pa_decode_ws")
     return out
+
+
+class KVManager:
+    """Host-side KV block manager (pa_kvm_* in the C ABI): a free list of
+    blocks, reference-counted sharing and per-sequence block tables.  Pure
+    host code -- usable without a GPU."""
+
+    def __init__(self, num_blocks, block_size=16, max_blocks_per_seq=128, shuffle_seed=0):
+        self._l = lib()
+        self._h = self._l.pa_kvm_create(num_blocks, block_size, max_blocks_per_seq,
+                                        ctypes.c_uint64(shuffle_seed))
+        if not self._h:
+            raise PaError(-2, "pa_kvm_create: invalid sizes")
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self.max_blocks_per_seq = max_blocks_per_seq
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._l.pa_kvm_destroy(h)
+
+    @staticmethod
+    def _out():
+        return ctypes.c_int32(-1)
+
+    def add_sequence(self, num_tokens, parent=-1, shared_blocks=0) -> int:
+        sid = self._out()
+        _check(self._l.pa_kvm_add_sequence(self._h, num_tokens, parent, shared_blocks,
+                                           ctypes.byref(sid)), "pa_kvm_add_sequence")
+        return sid.value
+
+    def fork(self, parent) -> int:
+        sid = self._out()
+        _check(self._l.pa_kvm_fork(self._h, parent, ctypes.byref(sid)), "pa_kvm_fork")
+        return sid.value
+
+    def append(self, seq):
+        """(slot, copy_src, copy_dst); copy_src = copy_dst = -1 unless the
+        token lands in a shared block (copy-on-write)."""
+        slot, src, dst = self._out(), self._out(), self._out()
+        _check(self._l.pa_kvm_append(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                     ctypes.byref(dst)), "pa_kvm_append")
+        return slot.value, src.value, dst.value
+
+    def free(self, seq):
+        _check(self._l.pa_kvm_free(self._h, seq), "pa_kvm_free")
+
+    def context_len(self, seq) -> int:
+        return self._l.pa_kvm_context_len(self._h, seq)
+
+    def slot(self, seq, token) -> int:
+        out = self._out()
+        _check(self._l.pa_kvm_slot(self._h, seq, token, ctypes.byref(out)), "pa_kvm_slot")
+        return out.value
+
+    def num_free_blocks(self) -> int:
+        return self._l.pa_kvm_num_free_blocks(self._h)
+
+    def refcount(self, block) -> int:
+        return self._l.pa_kvm_refcount(self._h, block)
+
+    def block_tables(self, seqs, row_len=None):
+        """(tables [n, row_len] int32, context_lens [n] int32) for the batch
+        rows `seqs` (a negative id gives an empty padding row)."""
+        import numpy as np
+        row_len = row_len or self.max_blocks_per_seq
+        ids = np.ascontiguousarray(seqs, dtype=np.int32)
+        tables = np.empty((len(ids), row_len), np.int32)
+        lens = np.empty(len(ids), np.int32)
+        _check(self._l.pa_kvm_block_tables(self._h, ids.ctypes.data, len(ids),
+                                           tables.ctypes.data, row_len, lens.ctypes.data),
+               "pa_kvm_block_tables")
+        return tables, lens
 
 
 def device_errors(stream=None, device=None) -> int:

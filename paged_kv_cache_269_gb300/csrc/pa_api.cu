@@ -331,6 +331,7 @@ const char *pa_status_string(int status) {
         case PA_ERR_ALIGN: return "fp16 pointer not 16-byte aligned";
         case PA_ERR_WORKSPACE: return "workspace or counter buffer missing, too small or misaligned";
         case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_OUT_OF_BLOCKS: return "KV cache exhausted: no free block";
         default: return "unknown status";
     }
 }

@@ -1,0 +1,117 @@
+"""A continuously batched decode loop over the host-side KV block manager.
+
+Sequences join (some sharing a system prompt's blocks, some forked from a
+parent as parallel samples), grow by one token per step, and finish; the
+manager hands out slots and copy-on-write copies, the step writes the new K/V
+and decodes.  After every step the output is compared with the oracle run on a
+host mirror of the cache that receives the same copies and writes.  The loop
+runs eagerly and replayed from a CUDA graph."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+H, D, B, N, MB, SMAX = 4, 128, 16, 1024, 64, 16
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_269_gb300 as pa
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    pa.lib()
+    pa.device_errors()
+    return d
+
+
+def _normal(rng, shape):
+    return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+
+
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_continuous_batching_loop(dev, use_graph):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    from paged_kv_cache_269_gb300.step import DecodeStep
+    rng = np.random.default_rng(77 + use_graph)
+    mgr = pa.KVManager(N, B, MB, shuffle_seed=5)
+    mirror_k = np.full((N, H, B, D), np.nan, np.float16)
+    mirror_v = np.full_like(mirror_k, np.nan)
+    kc = torch.from_numpy(mirror_k).to(dev)
+    vc = torch.from_numpy(mirror_v).to(dev)
+    scale = float(np.float32(1 / np.sqrt(D)))
+    step = DecodeStep(kc, vc, SMAX, MB, scale, use_graph=use_graph, partition_tokens=64)
+
+    def write(slots, k, v):
+        """Store token K/V at slots on the device and in the mirror."""
+        nonlocal mirror_k, mirror_v
+        slots = np.asarray(slots, np.int32)
+        with torch.cuda.stream(step.stream):     # ordered with the steps
+            ts = torch.from_numpy(slots).to(dev)
+            pa.reshape_and_cache(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), kc, vc,
+                                 ts)
+        mirror_k, mirror_v = oracle.reshape_and_cache(k, v, mirror_k, mirror_v, slots)
+
+    def prefill(seq, first):
+        n = mgr.context_len(seq)
+        if n > first:
+            slots = [mgr.slot(seq, t) for t in range(first, n)]
+            write(slots, _normal(rng, (n - first, H, D)), _normal(rng, (n - first, H, D)))
+
+    running = []
+    system = mgr.add_sequence(80)                 # a 5-block system prompt
+    prefill(system, 0)
+    running.append(system)
+    for _ in range(3):                            # requests sharing its full blocks
+        s = mgr.add_sequence(80 + int(rng.integers(1, 40)), system, 5)
+        prefill(s, 80)
+        running.append(s)
+    running.append(mgr.fork(running[1]))          # parallel samples of request 1
+    running.append(mgr.fork(running[1]))
+    s = mgr.add_sequence(int(rng.integers(1, 300)))
+    prefill(s, 0)
+    running.append(s)
+
+    for it in range(40):
+        # continuous batching: some sequences finish, new ones join
+        if it % 7 == 6 and len(running) > 3:
+            mgr.free(running.pop(int(rng.integers(0, len(running)))))
+        if it % 5 == 4 and len(running) < SMAX:
+            parent = running[int(rng.integers(0, len(running)))]
+            if rng.random() < 0.5:
+                running.append(mgr.fork(parent))
+            else:
+                s = mgr.add_sequence(int(rng.integers(1, 200)))
+                prefill(s, 0)
+                running.append(s)
+        slots, cow = [], []
+        for s in running:
+            slot, src, dst = mgr.append(s)
+            slots.append(slot)
+            if src >= 0:
+                cow.append((src, dst))
+        if cow:
+            step.copy_on_write(cow)
+            mirror_k, mirror_v = oracle.copy_blocks(mirror_k, mirror_v, mirror_k, mirror_v,
+                                                    np.asarray(cow, np.int32))
+        n = len(running)
+        q, kn, vn = (_normal(rng, (n, H, D)) for _ in range(3))
+        tables, lens = mgr.block_tables(running, MB)
+        step.prepare(q, kn, vn, np.asarray(slots, np.int32), tables, lens)
+        out = step.launch()
+        step.stream.synchronize()
+        got = out[:n].cpu().numpy()
+        mirror_k, mirror_v = oracle.reshape_and_cache(kn, vn, mirror_k, mirror_v,
+                                                      np.asarray(slots, np.int32))
+        ref = oracle.decode(q, mirror_k, mirror_v, tables, lens, scale)
+        assert_parity(got, ref, f"step {it} (graph={use_graph})")
+        assert (out[n:].cpu().numpy() == 0).all()          # padding rows
+    assert pa.device_errors(stream=step.stream) == 0
+    assert np.array_equal(kc.cpu().numpy().view(np.uint16), mirror_k.view(np.uint16))

@@ -66,6 +66,9 @@ def load(path: str = _LIB_PATH, src: str = _SRC):
     lib.oracle_reshape_and_cache.argtypes = [u16p, u16p, u16p, u16p, i32p,
                                              ci, ci, ci, ci, ci]
     lib.oracle_reshape_and_cache.restype = ci
+    lib.oracle_prefill.argtypes = [dp, u16p, u16p, u16p, i32p, i32p, i32p, ctypes.c_double,
+                                   ci, ci, ci, ci, ci, ci, ci]
+    lib.oracle_prefill.restype = ci
     lib.oracle_copy_blocks.argtypes = [u16p, u16p, ci, u16p, u16p, ci, i32p, ci, ci, ci, ci]
     lib.oracle_copy_blocks.restype = ci
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
@@ -148,6 +151,29 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, lib=None):
     if rc != 0:
         raise OracleError(ERRORS.get(rc, str(rc)))
     return kc, vc
+
+
+def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+            lib=None, dtype: str = "f16") -> np.ndarray:
+    """fp64 causal attention output [total_q, H, D]: sequence s's queries are
+    rows query_start[s] .. query_start[s+1]-1 of q, the last tokens of its
+    context, each attending to keys 0 .. its own position."""
+    lib = lib or _get()
+    T, H, D = q.shape
+    N, H2, B, D2 = k_cache.shape
+    if (H2, D2) != (H, D) or v_cache.shape != k_cache.shape:
+        raise OracleError("shape mismatch")
+    S = int(np.asarray(context_lens).shape[0])
+    MB = block_tables.shape[1]
+    out = np.zeros((T, H, D), dtype=np.float64)
+    keep = [_u16(q), _u16(k_cache), _u16(v_cache), _i32(block_tables), _i32(context_lens),
+            _i32(query_start)]
+    rc = lib.oracle_prefill(out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                            keep[0][1], keep[1][1], keep[2][1], keep[3][1], keep[4][1], keep[5][1],
+                            float(scale), S, H, D, B, N, max(1, MB), DTYPES[dtype])
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, str(rc)))
+    return out
 
 
 def copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs, lib=None):

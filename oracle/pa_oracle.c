@@ -289,3 +289,105 @@ int oracle_copy_blocks(const uint16_t *src_k, const uint16_t *src_v, int src_num
     }
     return ORACLE_OK;
 }
+
+/*
+ * Paged prefill: causal multi-query attention over the paged cache.
+ *
+ * Sequence s has q_len_s = query_start[s + 1] - query_start[s] query rows
+ * (rows query_start[s] .. query_start[s + 1] - 1 of q and out), which are the
+ * last q_len_s tokens of its context: query i sits at position
+ * p = ctx_s - q_len_s + i and attends to keys 0 .. p of the sequence
+ * ("vLLM 2026 推理引擎全解", §1.3: prefill processes the prompt, computing many
+ * positions at once; §1.1: o_t = Attention(q_t, K_{1:t}, V_{1:t}) for each t).
+ * Their K/V are already in the cache.
+ *
+ * out          [total_q, num_heads, head_dim] double (written)
+ * q            [total_q, num_heads, head_dim] 16-bit element bits
+ * query_start  [num_seqs + 1] int32, non-decreasing, query_start[0] = 0
+ * Other arrays and dtype as oracle_decode.  Returns ORACLE_BAD_CONTEXT if a
+ * sequence has more queries than tokens.
+ */
+int oracle_prefill(double *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                   const int32_t *block_tables, const int32_t *context_lens,
+                   const int32_t *query_start, double scale, int num_seqs, int num_heads,
+                   int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int dtype)
+{
+    if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || max_blocks_per_seq <= 0 ||
+        (dtype != ORACLE_F16 && dtype != ORACLE_BF16) || (num_seqs > 0 && query_start[0] != 0))
+        return ORACLE_BAD_ARG;
+    for (int s = 0; s < num_seqs; ++s) {
+        int ctx = context_lens[s];
+        int q_len = query_start[s + 1] - query_start[s];
+        if (ctx < 0 || (int64_t)ctx > (int64_t)max_blocks_per_seq * block_size || q_len < 0 ||
+            q_len > ctx)
+            return ORACLE_BAD_CONTEXT;
+        for (int b = 0; b < (ctx + block_size - 1) / block_size; ++b) {
+            int32_t phys = block_tables[(size_t)s * max_blocks_per_seq + b];
+            if (phys < 0 || phys >= num_blocks)
+                return ORACLE_BAD_TABLE;
+        }
+    }
+
+    int failed = 0;
+    int num_pairs = num_seqs * num_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int pair = 0; pair < num_pairs; ++pair) {
+        int s = pair / num_heads;
+        int h = pair % num_heads;
+        int ctx = context_lens[s];
+        int q_first = query_start[s];
+        int q_len = query_start[s + 1] - q_first;
+        if (q_len == 0)
+            continue;
+        double *K = malloc(sizeof(double) * (size_t)ctx * head_dim);
+        double *V = malloc(sizeof(double) * (size_t)ctx * head_dim);
+        double *qd = malloc(sizeof(double) * (size_t)head_dim);
+        double *weights = malloc(sizeof(double) * (size_t)ctx);
+        if (!K || !V || !qd || !weights) {
+            free(K); free(V); free(qd); free(weights);
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        /* gather the sequence's K and V through its block table */
+        for (int t = 0; t < ctx; ++t) {
+            int64_t phys = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+            int offset = t % block_size;
+            for (int d = 0; d < head_dim; ++d) {
+                size_t at = cache_index(phys, h, offset, d, num_heads, block_size, head_dim);
+                K[(size_t)t * head_dim + d] = element_to_double(k_cache[at], dtype);
+                V[(size_t)t * head_dim + d] = element_to_double(v_cache[at], dtype);
+            }
+        }
+        for (int i = 0; i < q_len; ++i) {
+            size_t row = ((size_t)(q_first + i) * num_heads + h) * head_dim;
+            int pos = ctx - q_len + i;               /* this query's position */
+            for (int d = 0; d < head_dim; ++d)
+                qd[d] = element_to_double(q[row + d], dtype);
+            double max_score = -INFINITY;
+            for (int t = 0; t <= pos; ++t) {          /* causal: keys 0 .. pos */
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    dot += qd[d] * K[(size_t)t * head_dim + d];
+                weights[t] = scale * dot;
+                if (weights[t] > max_score)
+                    max_score = weights[t];
+            }
+            double total = 0.0;
+            for (int t = 0; t <= pos; ++t) {
+                weights[t] = exp(weights[t] - max_score);
+                total += weights[t];
+            }
+            for (int d = 0; d < head_dim; ++d)
+                out[row + d] = 0.0;
+            for (int t = 0; t <= pos; ++t) {
+                double w = weights[t] / total;
+                for (int d = 0; d < head_dim; ++d)
+                    out[row + d] += w * V[(size_t)t * head_dim + d];
+            }
+        }
+        free(K); free(V); free(qd); free(weights);
+    }
+    return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}

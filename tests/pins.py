@@ -385,6 +385,81 @@ def pin_copy_blocks(lib):
     assert np.array_equal(_decode(lib, case, k_cache=k2, v_cache=v2, block_tables=t2), base)
 
 
+def brute_force_prefill(q, kc, vc, tables, lens, qs, scale):
+    """Pure-Python causal attention: query i of sequence s sits at position
+    ctx - q_len + i and sees keys 0 .. that position."""
+    T, H, D = q.shape
+    B = kc.shape[2]
+    out = np.zeros((T, H, D))
+    for s in range(len(lens)):
+        ctx, q_len = int(lens[s]), int(qs[s + 1] - qs[s])
+        for h in range(H):
+            rows_k = [[float(x) for x in kc[int(tables[s][t // B]), h, t % B]] for t in range(ctx)]
+            rows_v = [[float(x) for x in vc[int(tables[s][t // B]), h, t % B]] for t in range(ctx)]
+            for i in range(q_len):
+                row = int(qs[s]) + i
+                pos = ctx - q_len + i
+                qv = [float(x) for x in q[row, h]]
+                e = [math.exp(scale * math.fsum(a * b for a, b in zip(qv, rows_k[t])))
+                     for t in range(pos + 1)]
+                z = math.fsum(e)
+                for d in range(D):
+                    out[row, h, d] = math.fsum(e[t] * rows_v[t][d] for t in range(pos + 1)) / z
+    return out
+
+
+def _prefill(lib, case, **over):
+    args = dict(q=case.q, k_cache=case.k_cache, v_cache=case.v_cache,
+                block_tables=case.block_tables, context_lens=case.context_lens,
+                query_start=case.query_start, scale=case.scale, dtype=case.dtype)
+    args.update(over)
+    return oracle.prefill(lib=lib, **args)
+
+
+def pin_prefill_brute_force(lib):
+    case = workloads.build_prefill_case("pbf", [1, 20, 37, 16], [1, 20, 5, 16], num_heads=2,
+                                        head_dim=8, seed=31, spare_frac=0.5)
+    got = _prefill(lib, case)
+    ref = brute_force_prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
+                              case.context_lens, case.query_start, case.scale)
+    assert_close(got, ref, 1e-12, "prefill brute force")
+
+
+def pin_prefill_library_attention(lib):
+    """fp64 torch attention with an explicit causal mask on numpy-gathered K/V."""
+    import torch
+    case = workloads.build_prefill_case("plib", [70, 130], [70, 40], num_heads=3, head_dim=32,
+                                        seed=32)
+    got = _prefill(lib, case)
+    for s in range(case.num_seqs):
+        ctx, q0 = int(case.context_lens[s]), int(case.query_start[s])
+        q_len = int(case.query_start[s + 1]) - q0
+        for h in range(case.num_heads):
+            K, V = gather_contiguous((case.k_cache, case.v_cache, case.block_tables,
+                                      case.context_lens, case.block_size), s, h)
+            Q = case.q[q0:q0 + q_len, h].astype(np.float64)
+            pos = np.arange(ctx - q_len, ctx)[:, None]
+            mask = torch.from_numpy(np.arange(ctx)[None, :] <= pos)
+            o = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(Q)[None, None], torch.from_numpy(K)[None, None],
+                torch.from_numpy(V)[None, None], attn_mask=mask[None, None], scale=case.scale)
+            assert_close(got[q0:q0 + q_len, h], o[0, 0].numpy(), 1e-12, "prefill vs library")
+
+
+def pin_prefill_special_cases(lib):
+    # one query per sequence, at the last position, is decode
+    case = workloads.build_prefill_case("p1", [33, 90, 5], [1, 1, 1], num_heads=2, head_dim=16,
+                                        seed=33)
+    got = _prefill(lib, case)
+    dec = _decode(lib, case)
+    assert np.array_equal(got, dec), "a single query must match decode"
+    # the first query of a whole-prompt prefill sees only token 0: its V row
+    case = workloads.build_prefill_case("p2", [40], [40], num_heads=2, head_dim=16, seed=34)
+    got = _prefill(lib, case)
+    phys = case.block_tables[0, 0]
+    assert np.array_equal(got[0], case.v_cache[phys, :, 0, :].astype(np.float64))
+
+
 PINS = [
     ("half_decoding", pin_half_decoding),
     ("bf16_decoding", pin_bf16_decoding),
@@ -402,4 +477,7 @@ PINS = [
     ("masking", pin_masking),
     ("reshape_and_cache", pin_reshape_and_cache),
     ("copy_blocks", pin_copy_blocks),
+    ("prefill_brute_force", pin_prefill_brute_force),
+    ("prefill_library_attention", pin_prefill_library_attention),
+    ("prefill_special_cases", pin_prefill_special_cases),
 ]

@@ -39,18 +39,49 @@ MUTATIONS = {
                        "int offset = (slot + 1) % block_size;\n        for (int h = 0; h < num_heads; ++h) {"),
     "reshape_skips_zero": ("if (slot < 0)\n            continue;", "if (slot <= 0)\n            continue;"),
     "reshape_k_only": ("v_cache[dst] = v[src];", "v_cache[dst] = k[src];"),
+    "prefill_not_causal": ("int pos = ctx - q_len + i;               /* this query's position */",
+                           "int pos = ctx - 1;"),
+    "prefill_position": ("int pos = ctx - q_len + i;               /* this query's position */",
+                         "int pos = ctx - q_len + i - (i > 0);"),
     "copy_v_from_k": ("dst_v[to] = src_v[from];", "dst_v[to] = src_k[from];"),
     "copy_wrong_head": ("size_t to = cache_index(dst, h, t, d,", "size_t to = cache_index(dst, 0, t, d,"),
 }
+
+
+# Mutations of lines that appear in more than one function name the function
+# whose copy they change.
+IN_FUNCTION = {
+    "drop_scale": "oracle_decode", "softmax_sign": "oracle_decode",
+    "no_normalisation": "oracle_decode", "offset_shift": "oracle_decode",
+    "logical_block": "oracle_decode", "k_from_v": "oracle_decode",
+    "q_wrong_head": "oracle_decode", "head_offset_transposed": "oracle_decode",
+    "prefill_drop_scale": "oracle_prefill", "prefill_softmax_sign": "oracle_prefill",
+    "prefill_k_from_v": "oracle_prefill", "prefill_offset_shift": "oracle_prefill",
+}
+MUTATIONS.update({
+    "prefill_drop_scale": ("weights[t] = scale * dot;", "weights[t] = dot;"),
+    "prefill_softmax_sign": ("exp(weights[t] - max_score)", "exp(max_score - weights[t])"),
+    "prefill_k_from_v": ("K[(size_t)t * head_dim + d] = element_to_double(k_cache[at], dtype);",
+                         "K[(size_t)t * head_dim + d] = element_to_double(v_cache[at], dtype);"),
+    "prefill_offset_shift": ("int offset = t % block_size;", "int offset = (t + 1) % block_size;"),
+})
+
+
+def function_span(text, name):
+    start = text.index("\nint " + name + "(")
+    end = text.index("\n}\n", start) + 3
+    return start, end
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_mutation_is_caught(name, tmp_path):
     old, new = MUTATIONS[name]
     text = open(SRC, encoding="utf-8").read()
-    assert text.count(old) == 1, f"mutation {name} no longer matches the oracle source"
+    lo, hi = function_span(text, IN_FUNCTION[name]) if name in IN_FUNCTION else (0, len(text))
+    body = text[lo:hi]
+    assert body.count(old) == 1, f"mutation {name} no longer matches the oracle source"
     src = tmp_path / "mutant.c"
-    src.write_text(text.replace(old, new), encoding="utf-8")
+    src.write_text(text[:lo] + body.replace(old, new) + text[hi:], encoding="utf-8")
     lib = oracle.load(path=str(tmp_path / "libmutant.so"), src=str(src))
     caught = []
     for pin_name, fn in PINS:

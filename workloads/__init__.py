@@ -77,6 +77,9 @@ class DecodeCase:
     shared_prefix_blocks: int = 0
     meta: dict = field(default_factory=dict)
     dtype: str = "f16"
+    # prefill cases: q holds total_q rows; sequence s owns rows
+    # query_start[s] .. query_start[s + 1] - 1, its last tokens
+    query_start: Optional[np.ndarray] = None
 
     @property
     def num_seqs(self) -> int:
@@ -254,6 +257,59 @@ def build_case(name: str, context_lens, *, num_heads: int, head_dim: int,
     if new_tokens:
         add_new_tokens(case)
     return case
+
+
+def build_prefill_case(name: str, context_lens, query_lens, *, num_heads: int, head_dim: int,
+                       seed: int, **kw) -> DecodeCase:
+    """A prefill batch: sequence s has context_lens[s] tokens in the cache, of
+    which the last query_lens[s] are the queries (a chunk of its prompt, or
+    all of it).  q is [sum(query_lens), H, D]."""
+    ql = np.asarray(query_lens, dtype=np.int32)
+    case = build_case(name, context_lens, num_heads=num_heads, head_dim=head_dim, seed=seed, **kw)
+    if (ql > case.context_lens).any() or (ql < 0).any():
+        raise ValueError("query_lens must lie in [0, context_lens]")
+    qs = np.zeros(len(ql) + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(ql)
+    q = np.empty((int(qs[-1]), num_heads, head_dim), dtype=case.q.dtype)
+    fill_normal(q, seed, 6)
+    case.q = q
+    case.query_start = qs
+    return case
+
+
+PREFILL_WORKLOADS = ("prefill_llama7b", "prefill_chunked")
+
+
+def make_prefill_workload(kind: str, seed: Optional[int] = None, **kw) -> DecodeCase:
+    """prefill_llama7b  16 prompts of 1024 tokens each, prefilled whole, on a
+                        LLaMA-7B layer (32 heads x 128).
+    prefill_chunked     32 sequences with contexts U[512, 4096] whose last
+                        256 tokens are a prompt chunk being prefilled."""
+    seeds = {"prefill_llama7b": 21, "prefill_chunked": 22}
+    if kind not in seeds:
+        raise KeyError(kind)
+    seed = seeds[kind] if seed is None else seed
+    rng = np.random.default_rng(np.random.SeedSequence(seed, spawn_key=(0,)))
+    if kind == "prefill_llama7b":
+        ctx = np.full(16, 1024)
+        return build_prefill_case(kind, ctx, ctx, num_heads=32, head_dim=128, seed=seed,
+                                  max_blocks_per_seq=64, **kw)
+    ctx = rng.integers(512, 4096, size=32, endpoint=True)
+    return build_prefill_case(kind, ctx, np.full(32, 256), num_heads=32, head_dim=128, seed=seed,
+                              max_blocks_per_seq=256, **kw)
+
+
+def prefill_algorithmic_flops(case: DecodeCase) -> int:
+    """2 * D flops per (query, key) for q.k and again for p.V, over the
+    causal pairs: query at position p sees p + 1 keys."""
+    total = 0
+    for s in range(case.num_seqs):
+        ctx = int(case.context_lens[s])
+        q_len = int(case.query_start[s + 1] - case.query_start[s])
+        first = ctx - q_len
+        keys = q_len * (first + 1) + q_len * (q_len - 1) // 2
+        total += keys
+    return 4 * case.head_dim * case.num_heads * total
 
 
 def add_new_tokens(case: DecodeCase) -> None:

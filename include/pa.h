@@ -179,6 +179,40 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int32_t max_blocks_per_seq, const pa_dims *dims, void *stream);
 
 /*
+ * pa_prefill -- causal multi-query attention over the paged cache (prefill).
+ *
+ * Source: prefill processes a prompt's tokens together and is compute-bound
+ * ("vLLM 2026 推理引擎全解", §1.3); each token attends to itself and the
+ * tokens before it, o_t = Attention(q_t, K_{1:t}, V_{1:t}) (same page, §1.1),
+ * with K/V gathered through the block table (§2.1-§2.2).  Runs on the tcgen05
+ * tensor cores (S = Q K^T and P V in tensor memory).
+ *
+ *   out           device, [total_query_tokens, H, D] (written)
+ *   q             device, [total_query_tokens, H, D]
+ *   k_cache, v_cache, block_tables, context_lens: as pa_decode; the queries'
+ *                 own K/V must already be in the cache (pa_reshape_and_cache)
+ *   query_start   device, int32 [S + 1]: sequence s owns query rows
+ *                 query_start[s] .. query_start[s + 1] - 1, which are the last
+ *                 q_len_s = query_start[s + 1] - query_start[s] tokens of its
+ *                 context (a whole prompt, or its latest chunk)
+ *   total_query_tokens  host: rows of q and out
+ *   max_query_len host: an upper bound of every q_len_s (sizes the grid)
+ *   scale, max_blocks_per_seq, dims, stream: as pa_decode
+ *
+ * Query i of sequence s sits at position p = ctx_s - q_len_s + i and
+ * attends to keys 0 .. p.  Built for head_dim 128, block_size 16, fp16 or
+ * bf16 (PA_ERR_UNSUPPORTED otherwise).  Scores and softmax are fp32; the
+ * probabilities enter the P V product as a pair of 16-bit values (P_hi +
+ * P_lo) so the product keeps about 22 bits.  A sequence with q_len_s >
+ * ctx_s, ctx_s > max_blocks_per_seq * B, or rows outside
+ * [0, total_query_tokens) is skipped and flags PA_DEVERR_CONTEXT.
+ */
+int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+               const int32_t *block_tables, const int32_t *context_lens,
+               const int32_t *query_start, int32_t total_query_tokens, int32_t max_query_len,
+               float scale, int32_t max_blocks_per_seq, const pa_dims *dims, void *stream);
+
+/*
  * Bytes of partial-result workspace pa_decode_ws needs for these sizes and
  * partition length (partition_tokens = 0 selects the default).  0 means no
  * partials are needed (every sequence fits one partition).  Returns

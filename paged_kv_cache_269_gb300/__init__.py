@@ -20,7 +20,8 @@ import threading
 
 from . import build as _build
 
-__all__ = ["PaError", "Dims", "KVManager", "lib", "reshape_and_cache", "copy_blocks", "decode", "decode_workspace_bytes",
+__all__ = ["PaError", "Dims", "KVManager", "lib", "reshape_and_cache", "copy_blocks", "decode",
+           "prefill", "decode_workspace_bytes",
            "decode_counters_bytes", "device_errors", "reset_workspaces", "version", "DEVERR_TABLE", "DEVERR_CONTEXT",
            "DEVERR_SLOT", "DEVERR_TIMEOUT"]
 
@@ -34,7 +35,8 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_UNSUPPO
           -7: "PA_ERR_OUT_OF_BLOCKS"}
 
 # Every symbol include/pa.h declares.
-EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_bytes",
+EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill",
+           "pa_decode_workspace_bytes",
            "pa_decode_counters_bytes", "pa_decode_ws", "pa_decode_static", "pa_device_errors",
            "pa_status_string", "pa_last_cuda_error", "pa_version",
            "pa_kvm_create", "pa_kvm_destroy", "pa_kvm_num_free_blocks", "pa_kvm_refcount",
@@ -69,6 +71,7 @@ def _declare(l):
     l.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, dp, vp]
     l.pa_copy_blocks.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, dp, vp]
     l.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp]
+    l.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, dp, vp]
     l.pa_decode_workspace_bytes.argtypes = [dp, i32, i32]
     l.pa_decode_workspace_bytes.restype = sz
     l.pa_decode_counters_bytes.argtypes = [dp]
@@ -100,7 +103,7 @@ def _declare(l):
                  "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free", "pa_kvm_context_len",
                  "pa_kvm_slot", "pa_kvm_block_tables"):
         getattr(l, name).restype = i32
-    for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_decode_ws",
+    for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", "pa_decode_ws",
                  "pa_device_errors",
                  "pa_last_cuda_error", "pa_version"):
         getattr(l, name).restype = ctypes.c_int
@@ -239,6 +242,40 @@ def copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
                                   dst_k.shape[0], _ptr(block_pairs), block_pairs.shape[0],
                                   ctypes.byref(dims), sh)
     _check(rc, "pa_copy_blocks")
+
+
+def prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+            max_query_len=None, stream=None):
+    """Causal attention of the last q_len_s tokens of each sequence over its
+    paged K/V (pa_prefill).  q, out [total_q, H, D]; query_start [S + 1]
+    int32 on the device; max_query_len bounds every q_len_s (computed from
+    query_start, with a device sync, when None)."""
+    torch = _torch()
+    _element_dtype(k_cache)
+    et = k_cache.dtype
+    _need(k_cache, "k_cache", et, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", et, 4, dev)
+    _need(q, "q", et, 3, dev)
+    _need(out, "out", et, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(query_start, "query_start", torch.int32, 1, dev)
+    N, H, B, D = k_cache.shape
+    S = context_lens.shape[0]
+    if out.shape != q.shape or q.shape[1:] != (H, D) or query_start.shape[0] != S + 1 \
+            or block_tables.shape[0] != S:
+        raise ValueError("prefill: inconsistent shapes")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max()) if S else 0
+    dims = _cache_dims(k_cache, S)
+    sh, _ = _stream_handle(dev, stream)
+    with torch.cuda.device(dev):
+        rc = lib().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                              _ptr(context_lens), _ptr(query_start), q.shape[0], int(max_query_len),
+                              float(scale), block_tables.shape[1], ctypes.byref(dims), sh)
+    _check(rc, "pa_prefill")
+    return out
 
 
 def decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, num_blocks,

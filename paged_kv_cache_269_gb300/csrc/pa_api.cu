@@ -124,6 +124,15 @@ int check_device_addressable(const void *p, int device) {
 
 int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
 
+int current_device_info(unsigned int **err, int *num_sms) {
+    DeviceState *st = nullptr;
+    const int rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    *err = st->err;
+    *num_sms = st->num_sms;
+    return PA_OK;
+}
+
 void workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t max_parts,
                       WorkspaceLayout *out) {
     const size_t pairs = static_cast<size_t>(num_seqs) * static_cast<size_t>(num_heads);
@@ -198,6 +207,47 @@ int pa_copy_blocks(const void *src_k, const void *src_v, int32_t src_num_blocks,
                            block_pairs, num_pairs, dims->num_heads, dims->head_dim,
                            dims->block_size, src_num_blocks, dst_num_blocks, st->num_sms, st->err,
                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+               const int32_t *block_tables, const int32_t *context_lens,
+               const int32_t *query_start, int32_t total_query_tokens, int32_t max_query_len,
+               float scale, int32_t max_blocks_per_seq, const pa_dims *dims, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != PA_OK) return rc;
+    if (!prefill_supported(dims->dtype, dims->head_dim, dims->block_size)) return PA_ERR_UNSUPPORTED;
+    if (total_query_tokens < 0 || max_query_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+    if (dims->num_seqs == 0 || total_query_tokens == 0 || max_query_len == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+        return PA_ERR_NULL;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PA_ERR_ALIGN;
+    if (!isfinite(scale)) return PA_ERR_SHAPE;
+    // tensor-map coordinates are 32-bit: every cache row and query row must fit
+    if (static_cast<long long>(dims->num_blocks) * dims->num_heads * dims->block_size > 0x7fffffffLL ||
+        static_cast<long long>(max_blocks_per_seq) * dims->block_size > 0x7fffffffLL ||
+        dims->num_heads > 65535 || dims->num_seqs > 65535)
+        return PA_ERR_SHAPE;
+    unsigned int *err = nullptr;
+    int sms = 0;
+    rc = current_device_info(&err, &sms);
+    if (rc != PA_OK) return rc;
+    PrefillArgs a;
+    a.out = static_cast<uint16_t *>(out);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start = query_start;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.num_seqs = dims->num_seqs;
+    a.num_heads = dims->num_heads;
+    a.num_blocks = dims->num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.total_q = total_query_tokens;
+    a.err = err;
+    const cudaError_t e = launch_prefill(a, q, k_cache, v_cache, dims->dtype, max_query_len,
+                                         static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;  // tensor maps could not be made
     return e == cudaSuccess ? PA_OK : fail_cuda(e);
 }
 

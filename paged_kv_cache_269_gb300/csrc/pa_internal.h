@@ -51,6 +51,29 @@ cudaError_t launch_copy_blocks(const uint16_t *src_k, const uint16_t *src_v, uin
                                int32_t src_num_blocks, int32_t dst_num_blocks, int num_sms,
                                unsigned int *err, cudaStream_t stream);
 
+// Arguments of one prefill launch (device pointers unless noted).
+struct PrefillArgs {
+    uint16_t *out;                 // [total_q, H, D]
+    const int32_t *block_tables;   // [S, max_blocks_per_seq]
+    const int32_t *context_lens;   // [S]
+    const int32_t *query_start;    // [S + 1]
+    float scale_log2;
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t num_blocks;
+    int32_t max_blocks_per_seq;
+    int32_t total_q;
+    unsigned int *err;
+};
+
+bool prefill_supported(int dtype, int head_dim, int block_size);
+cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k_cache,
+                           const void *v_cache, int dtype, int max_query_len,
+                           cudaStream_t stream);
+
+// SM count and device error word of the current device (set up on first use).
+int current_device_info(unsigned int **err, int *num_sms);
+
 // Record a CUDA error for pa_last_cuda_error() and return PA_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
 

@@ -1,0 +1,79 @@
+"""GPU parity of pa_prefill (tcgen05 tensor cores) against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import assert_parity, to_numpy, torch_dtype, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_269_gb300 as pa
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    pa.lib()
+    pa.device_errors()
+    return d
+
+
+def run_prefill(case, dev):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    d = upload(case, dev)
+    qs = torch.from_numpy(case.query_start).to(dev)
+    out = torch.full(case.q.shape, float("nan"), dtype=torch_dtype(case), device=dev)
+    pa.prefill(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], qs,
+               case.scale)
+    return to_numpy(out, case), pa.device_errors()
+
+
+CTX = [1, 15, 16, 17, 64, 65, 127, 128, 129, 300, 513]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("mode", ["whole", "chunk", "single"])
+def test_ragged_prefill(dev, dtype, mode):
+    ctx = np.array(CTX)
+    if mode == "whole":
+        ql = ctx                                   # the whole prompt
+    elif mode == "chunk":
+        ql = np.minimum(ctx, [1, 7, 16, 5, 64, 1, 100, 128, 129, 200, 257])
+    else:
+        ql = np.ones_like(ctx)                     # one query each (decode-like)
+    case = workloads.build_prefill_case(f"pf_{mode}", ctx, ql, num_heads=2, head_dim=128,
+                                        seed=40 + len(mode), dtype=dtype)
+    got, flags = run_prefill(case, dev)
+    assert flags == 0
+    ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
+                         case.context_lens, case.query_start, case.scale, dtype=dtype)
+    assert_parity(got, ref, f"prefill {mode} {dtype}", dtype=dtype)
+
+
+@pytest.mark.parametrize("kind", workloads.PREFILL_WORKLOADS)
+def test_prefill_workloads_full_size(dev, kind):
+    case = workloads.make_prefill_workload(kind)
+    got, flags = run_prefill(case, dev)
+    assert flags == 0
+    ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
+                         case.context_lens, case.query_start, case.scale)
+    assert_parity(got, ref, kind)
+
+
+def test_prefill_bad_query_count_is_reported(dev):
+    import paged_kv_cache_269_gb300 as pa
+    case = workloads.build_prefill_case("pf_bad", [40, 40], [40, 40], num_heads=2, head_dim=128,
+                                        seed=3)
+    lens = case.context_lens.copy()
+    lens[1] = 20                                   # fewer tokens than queries
+    case.context_lens = lens
+    got, flags = run_prefill(case, dev)
+    assert flags & pa.DEVERR_CONTEXT
+    ref = oracle.prefill(case.q[:40], case.k_cache, case.v_cache, case.block_tables[:1],
+                         case.context_lens[:1], case.query_start[:2], case.scale)
+    assert_parity(got[:40], ref, "the valid sequence is still computed")

@@ -47,10 +47,12 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--op", choices=["step", "copy_blocks", "swap_out", "swap_in"], default="step",
+    p.add_argument("--op", choices=["step", "copy_blocks", "swap_out", "swap_in", "prefill"],
+                   default="step",
                    help="step: reshape_and_cache + decode (the hot path); the others time "
                         "pa_copy_blocks on a 4096-block pool, 2048 random pairs")
-    p.add_argument("--workload", default="llama7b_b64", choices=workloads.WORKLOADS)
+    p.add_argument("--workload", default="llama7b_b64",
+                   choices=workloads.WORKLOADS + workloads.PREFILL_WORKLOADS)
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
                    help="element type of q, the caches and the output")
@@ -528,6 +530,62 @@ def run_copy_op(args, local_rank):
         "gpu_launches": args.steps}))
 
 
+def run_prefill_op(args, local_rank):
+    """Time pa_prefill on a prefill workload (tensor-core bound)."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = args.workload if args.workload in workloads.PREFILL_WORKLOADS else "prefill_llama7b"
+    case = workloads.make_prefill_workload(wl, dtype=args.dtype)
+
+    def t(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    q, kc, vc = t(case.q), t(case.k_cache), t(case.v_cache)
+    bt, cl, qs = t(case.block_tables), t(case.context_lens), t(case.query_start)
+    out = torch.empty_like(q)
+    max_q = int((case.query_start[1:] - case.query_start[:-1]).max())
+    stream = torch.cuda.Stream(dev)
+    call = lambda: pa.prefill(out, q, kc, vc, bt, cl, qs, case.scale, max_query_len=max_q,
+                              stream=stream)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize(dev)
+    assert pa.device_errors(stream=stream) == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = workloads.prefill_algorithmic_flops(case)
+    tflops = flops / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, src = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        peak, src = 1900.0, "fallback 1.9 PFLOP/s"
+    print(json.dumps({
+        "metric": "pa_prefill TFLOP/s", "value": round(tflops, 2), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "dtype": args.dtype, "data": "synthetic",
+        "config": {"workload": wl, "num_seqs": case.num_seqs, "num_heads": case.num_heads,
+                   "head_dim": case.head_dim, "query_tokens": int(case.query_start[-1]),
+                   "context_tokens": int(case.context_lens.sum())},
+        "tokens_per_s": round(int(case.query_start[-1]) / (ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "peak_source": src,
+                     "algorithmic_flops_per_launch": int(flops),
+                     "note": "algorithmic flops: 4*D per causal (query, key) pair per head; "
+                             "the kernel issues 1.5x (P V runs for P_hi and P_lo)"},
+        "gpu_launches": args.steps}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -535,6 +593,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.op == "prefill":
+        if rank == 0:
+            run_prefill_op(args, local_rank)
         return
     if args.op != "step":
         if rank == 0:

@@ -8,23 +8,35 @@
 // attention; §2.1-§2.2 for the block table).
 //
 // How: this is the one dense contraction of the paged cache, so it runs on
-// the 5th-generation tensor cores with accumulators in tensor memory.
-//  * One CTA per (tile of 128 queries, head, sequence); six warps.
-//  * Warp 4 (TMA): loads the Q tile once and, per tile of 64 keys, the four
-//    16-token K and V blocks named by the block table, each as two 2-D
+// the 5th-generation tensor cores with every accumulator in tensor memory.
+//  * One CTA per (pair of 128-query tiles, head, sequence); ten warps.  The
+//    two query tiles share every K/V tile and take turns on the tensor core:
+//    while one tile's softmax runs, the other tile's MMAs do.
+//  * Warp 8 (TMA): loads both Q tiles once and, per tile of 128 keys, the
+//    eight 16-token K and V blocks named by the block table as 2-D
 //    tensor-map boxes (64 dims x 16 tokens) that land directly in the
-//    128-byte-swizzled operand layouts; double-buffered.
-//  * Warp 5 (MMA): S = Q K^T (M 128, N 64, K 128) into TMEM columns 0-63;
-//    after the softmax warps publish P, PV = P_hi V + P_lo V (M 128, N 128,
-//    K 64, V as an MN-major operand) into TMEM columns 128-255.
-//  * Warps 0-3 (softmax): thread t owns query row t (the TMEM lane layout of
-//    an M = 128 accumulator), reads its 64 scores with tcgen05.ld, masks the
-//    causal and context boundary, keeps the running max / sum in fp32 and
-//    the output row in registers (rescaled each tile), and writes P to
-//    shared memory as a 16-bit pair P_hi + P_lo (P_lo = P - P_hi), which
-//    keeps P exact to about 22 bits so small outputs meet the same relative
-//    bound as decode.  Rows of V past the last key are zeroed before use
-//    (a zero weight times a NaN would still be NaN).
+//    128-byte-swizzled operand layouts; two stages each for K and V.  Rows
+//    of the last V tile past the last key are zeroed before use (a zero
+//    weight times a NaN from an unused slot would still be NaN).
+//  * Warp 9 (MMA): S_t = Q_t K^T (M 128, N 128, K 128) into tensor memory;
+//    once softmax t has published P_t, O_t += P_hi V + P_lo V (M 128, N 128,
+//    K 128; P read from tensor memory, V as an MN-major operand), then
+//    S_t of the next key tile.  Order per key tile j:
+//    PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
+//  * Warps 0-3 / 4-7 (softmax of tile 0 / 1): thread = query row (the
+//    tensor-memory lane of an M = 128 accumulator).  It reads its 128
+//    scores, masks the causal boundary, and turns them into weights
+//    2^(x - m + 6) in fp32, where x is the score in the log2 domain and m a
+//    running maximum that is only raised when a tile's maximum exceeds it
+//    by more than 8 (so weights stay below 2^14, inside fp16's range);
+//    raising it rescales O_t in tensor memory.  The weights go back into the
+//    same tensor-memory columns as a 16-bit pair P_hi + P_lo (P_hi is the
+//    weight truncated to the format's precision, P_lo the rounded
+//    remainder), which carries about 21 bits, so small outputs meet the
+//    same relative bound as decode.  The row sum stays in fp32; the
+//    epilogue divides O_t by it.
+//  * Tensor-memory columns: S_0/P_0 0-127, S_1/P_1 128-255, O_0 256-383,
+//    O_1 384-511 (the whole of the SM's tensor memory: one CTA per SM).
 //  * Every wait is bounded; tensor memory is released on every path.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -42,35 +54,44 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;             // head_dim
-constexpr int kBM = 128;            // query rows per CTA (MMA M)
-constexpr int kBN = 64;             // keys per tile
+constexpr int kBM = 128;            // query rows per tile (MMA M)
+constexpr int kTiles = 2;           // query tiles per CTA
+constexpr int kBN = 128;            // keys per tile
 constexpr int kB = 16;              // block_size
 constexpr int kBlocksPerTile = kBN / kB;
 constexpr int kStages = 2;
-constexpr int kThreads = 192;       // 4 softmax warps + TMA warp + MMA warp
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemS = 0;      // S: columns 0-63
-constexpr uint32_t kTmemPV = 128;   // PV: columns 128-255
+constexpr int kThreads = 320;       // 2 x 4 softmax warps + TMA warp + MMA warp
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;      // S_t / P_t: columns 128 t .. 128 t + 127
+constexpr uint32_t kTmemO = 256;    // O_t: columns 256 + 128 t .. 256 + 128 t + 127
+constexpr float kRescaleLog2 = 8.f; // raise the running maximum only past this margin
+constexpr float kBiasLog2 = 6.f;    // weights are 2^(x - m + 6): at most 2^14
 
 // shared memory layout (bytes; tiles 1024-aligned for the 128B swizzle)
-constexpr int kHalfRowsQ = kBM * 128;          // one 64-dim half of Q: 128 rows x 128 B
-constexpr int OFF_Q = 0;                       // [2 halves][128 rows][128 B]
-constexpr int kTileKV = 2 * kBN * 128;         // K or V tile: 2 halves x 64 keys x 128 B
-constexpr int OFF_K = OFF_Q + 2 * kHalfRowsQ;  // [stage][half][64 keys][128 B]
-constexpr int OFF_V = OFF_K + kStages * kTileKV;
-constexpr int kTileP = kBM * 128;              // P: 128 rows x 64 keys x 2 B
-constexpr int OFF_PHI = OFF_V + kStages * kTileKV;
-constexpr int OFF_PLO = OFF_PHI + kTileP;
-constexpr int OFF_BAR = OFF_PLO + kTileP;
-constexpr int kNumBars = 12;
+constexpr int kHalf = 128 * 128;               // one 64-dim half of a 128-row tile
+constexpr int kTileBytes = 2 * kHalf;          // Q tile, K tile or V tile: 32 KiB
+constexpr int OFF_Q = 0;                       // [tile][half][128 rows][128 B]
+constexpr int OFF_K = OFF_Q + kTiles * kTileBytes;   // [stage][half][128 keys][128 B]
+constexpr int OFF_V = OFF_K + kStages * kTileBytes;
+constexpr int OFF_BAR = OFF_V + kStages * kTileBytes;
+enum Bar {
+    Q_FULL = 0,
+    K_FULL = 1,          // [stage]
+    K_EMPTY = 3,         // [stage]
+    V_FULL = 5,          // [stage]
+    V_EMPTY = 7,         // [stage]
+    V_ZERO = 9,          // last V tile loaded and its tail rows cleared
+    S_FULL = 10,         // [tile]
+    P_FULL = 12,         // [tile], one arrival per softmax warp
+    O_FULL = 14,         // [tile]
+    MMA_DONE = 16,
+    kNumBars = 17
+};
 constexpr int OFF_TMEM = OFF_BAR + kNumBars * 8;
 constexpr int OFF_FLAG = OFF_TMEM + 8;
 constexpr int kSmemBytes = OFF_FLAG + 8 + 1024;  // + alignment slack
-
-enum Bar { Q_FULL = 0, K_FULL = 1, V_FULL = 3, KV_EMPTY = 5, S_FULL = 7, S_EMPTY = 8, P_FULL = 9,
-           PV_FULL = 10, MMA_DONE = 11 };
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
@@ -90,12 +111,23 @@ __host__ __device__ constexpr uint32_t instr_desc(bool bf16, bool b_mn, int n) {
            (static_cast<uint32_t>(kBM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                        bool accumulate) {
+// D (tensor memory) [+]= A (shared memory) * B (shared memory)
+__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       bool accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0));
+}
+
+// D (tensor memory) [+]= A (tensor memory: row = lane, two 16-bit elements
+// per 32-bit column, lower k in the low half) * B (shared memory)
+__device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b,
+                                       uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0));
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -112,9 +144,8 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
-    uint32_t r[32];
+// 32 consecutive 32-bit columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t addr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -125,9 +156,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(addr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 / 32 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(addr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(addr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x by the hardware approximation (ex2.approx.ftz.f32: 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y,
@@ -148,26 +212,41 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, in
         : "memory");
 }
 
+// The weight pair (P_hi, P_lo) of two consecutive keys, packed as the MMA
+// reads A from tensor memory.  P_hi = the weight with its fp32 mantissa cut to
+// the 16-bit format's width (exact in that format for weights in its normal
+// range), P_lo = the remainder rounded to nearest.
 struct F16T {
     static constexpr bool kBf16 = false;
+    __device__ static __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+        const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+        const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+        const __half2 h = __floats2half2_rn(h0, h1);
+        const __half2 l = __floats2half2_rn(p0 - h0, p1 - h1);
+        hi = *reinterpret_cast<const uint32_t *>(&h);
+        lo = *reinterpret_cast<const uint32_t *>(&l);
+    }
     __device__ static __forceinline__ uint16_t round(float x) {
         const __half h = __float2half_rn(x);
         return *reinterpret_cast<const uint16_t *>(&h);
     }
-    __device__ static __forceinline__ float widen(uint16_t b) {
-        return __half2float(*reinterpret_cast<const __half *>(&b));
-    }
 };
 struct BF16T {
     static constexpr bool kBf16 = true;
+    __device__ static __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+        hi = __byte_perm(b0, b1, 0x7632);   // upper halves: the truncated bf16 values
+        const __nv_bfloat162 l = __floats2bfloat162_rn(p0 - __uint_as_float(b0 & 0xFFFF0000u),
+                                                       p1 - __uint_as_float(b1 & 0xFFFF0000u));
+        lo = *reinterpret_cast<const uint32_t *>(&l);
+    }
     __device__ static __forceinline__ uint16_t round(float x) {
         const __nv_bfloat16 b = __float2bfloat16_rn(x);
         return *reinterpret_cast<const uint16_t *>(&b);
     }
-    __device__ static __forceinline__ float widen(uint16_t b) {
-        return __uint_as_float(static_cast<uint32_t>(b) << 16);
-    }
 };
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 template <typename E>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -180,32 +259,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int s = blockIdx.z, h = blockIdx.y, qt = blockIdx.x;
+    // heaviest pairs (latest positions, most keys) are scheduled first
+    const int h = blockIdx.x, s = blockIdx.y, pair = gridDim.z - 1 - blockIdx.z;
     const int H = a.num_heads;
 
     grid_dependency_wait();
     allow_dependents_to_launch();
     const int q_first = a.query_start[s];
     const int q_len = a.query_start[s + 1] - q_first;
-    int ctx = a.context_lens[s];
-    const int row0 = qt * kBM;
+    const int ctx = a.context_lens[s];
+    const int row0 = pair * kTiles * kBM;
     if (q_len <= 0 || row0 >= q_len) return;  // nothing for this CTA (before any set-up)
     if (ctx > a.max_blocks_per_seq * kB || q_len > ctx || q_first < 0 ||
         q_first + q_len > a.total_q) {
         if (threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
         return;
     }
-    const int rows = min(kBM, q_len - row0);
-    const int first_pos = ctx - q_len + row0;     // position of tile row 0
-    const int kmax = first_pos + rows;            // keys 0 .. kmax-1 are needed
-    const int nkt = (kmax + kBN - 1) / kBN;       // key tiles
+    const int ntiles = q_len - row0 > kBM ? 2 : 1;
+    // tile t: rows row0 + 128 t ..; the last active tile needs the most keys
+    const int rows_last = min(kBM, q_len - row0 - (ntiles - 1) * kBM);
+    const int kmax = ctx - q_len + row0 + (ntiles - 1) * kBM + rows_last;  // keys 0 .. kmax-1
+    const int nkt = (kmax + kBN - 1) / kBN;
     const int nblk_needed = (kmax + kB - 1) / kB;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i)
-            mbar_init(&bar[i], i == S_EMPTY ? 4       // one arrival per softmax warp
-                               : i == P_FULL ? 128   // every softmax thread
-                                             : 1);
+            mbar_init(&bar[i], (i == P_FULL || i == P_FULL + 1) ? 4 : 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -222,58 +301,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA
-        uint32_t issued = 0;  // key tiles issued
+        int issued_k = 0, issued_v = 0;
         bool ok = true;
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bar[Q_FULL], 2 * kHalfRowsQ);
-            tma_load_3d(smem + OFF_Q, &tm_q, 0, h, q_first + row0, &bar[Q_FULL]);
-            tma_load_3d(smem + OFF_Q + kHalfRowsQ, &tm_q, 64, h, q_first + row0, &bar[Q_FULL]);
-            const int32_t *table = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
-            for (int j = 0; j < nkt; ++j) {
-                const int st = j % kStages;
-                if (!mbar_wait(&bar[KV_EMPTY + st], ((j / kStages) & 1) ^ 1, abort_flag, a.err)) {
-                    ok = false;
-                    break;
-                }
-                int phys[kBlocksPerTile];
-                int nvalid = 0;
-#pragma unroll
-                for (int i = 0; i < kBlocksPerTile; ++i) {
-                    const int b = j * kBlocksPerTile + i;
-                    phys[i] = -1;
-                    if (b < nblk_needed) {
-                        const int p = __ldg(table + b);
-                        if (static_cast<unsigned>(p) < static_cast<unsigned>(a.num_blocks)) {
-                            phys[i] = p;
-                            ++nvalid;
-                        } else {
-                            atomicOr(a.err, PA_DEVERR_TABLE);
-                        }
-                    }
-                }
-                uint8_t *kdst = smem + OFF_K + st * kTileKV;
-                uint8_t *vdst = smem + OFF_V + st * kTileKV;
-                mbar_arrive_expect_tx(&bar[K_FULL + st], nvalid * 2 * kB * 128);
-                mbar_arrive_expect_tx(&bar[V_FULL + st], nvalid * 2 * kB * 128);
-#pragma unroll
-                for (int i = 0; i < kBlocksPerTile; ++i) {
-                    if (phys[i] < 0) continue;
-                    const int y = (phys[i] * H + h) * kB;
-                    for (int half = 0; half < 2; ++half) {
-                        const int off = half * (kBN * 128) + i * (kB * 128);
-                        tma_load_2d(kdst + off, &tm_k, half * 64, y, &bar[K_FULL + st]);
-                        tma_load_2d(vdst + off, &tm_v, half * 64, y, &bar[V_FULL + st]);
-                    }
-                }
-                ++issued;
+            mbar_arrive_expect_tx(&bar[Q_FULL], ntiles * kTileBytes);
+            for (int t = 0; t < ntiles; ++t)
+                for (int half = 0; half < 2; ++half)
+                    tma_load_3d(smem + OFF_Q + t * kTileBytes + half * kHalf, &tm_q, half * 64, h,
+                                q_first + row0 + t * kBM, &bar[Q_FULL]);
+        }
+        const int32_t *table = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
+        for (int j = 0; j < nkt && ok; ++j) {
+            const int st = j % kStages;
+            const uint32_t ph = (j / kStages) & 1;
+            // physical blocks of this key tile: lane i < 8 looks up block i
+            int phys = -1;
+            const int b = j * kBlocksPerTile + lane;
+            if (lane < kBlocksPerTile && b < nblk_needed) {
+                const int p = __ldg(table + b);
+                if (static_cast<unsigned>(p) < static_cast<unsigned>(a.num_blocks))
+                    phys = p;
+                else
+                    atomicOr(a.err, PA_DEVERR_TABLE);
             }
-            if (!ok) {  // let every copy already issued land
-                mbar_wait_drain(&bar[Q_FULL], 0);
-                for (uint32_t j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
-                    mbar_wait_drain(&bar[K_FULL + j % kStages], (j / kStages) & 1);
-                    mbar_wait_drain(&bar[V_FULL + j % kStages], (j / kStages) & 1);
-                }
+            const unsigned valid_mask = __ballot_sync(0xffffffffu, phys >= 0);
+            const uint32_t bytes = __popc(valid_mask) * 2u * kB * 128u;
+            const int y = (phys * H + h) * kB;
+            ok = warp_all(mbar_wait(&bar[K_EMPTY + st], ph ^ 1, abort_flag, a.err));
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bar[K_FULL + st], bytes);
+            __syncwarp();
+            if (phys >= 0) {
+                uint8_t *dst = smem + OFF_K + st * kTileBytes + lane * (kB * 128);
+                tma_load_2d(dst, &tm_k, 0, y, &bar[K_FULL + st]);
+                tma_load_2d(dst + kHalf, &tm_k, 64, y, &bar[K_FULL + st]);
             }
+            ++issued_k;
+            ok = warp_all(mbar_wait(&bar[V_EMPTY + st], ph ^ 1, abort_flag, a.err));
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bar[V_FULL + st], bytes);
+            __syncwarp();
+            if (phys >= 0) {
+                uint8_t *dst = smem + OFF_V + st * kTileBytes + lane * (kB * 128);
+                tma_load_2d(dst, &tm_v, 0, y, &bar[V_FULL + st]);
+                tma_load_2d(dst + kHalf, &tm_v, 64, y, &bar[V_FULL + st]);
+            }
+            ++issued_v;
+            if (j == nkt - 1) {
+                // clear V rows kmax .. end of the tile once the loads have landed
+                ok = warp_all(mbar_wait(&bar[V_FULL + st], ph, abort_flag, a.err));
+                if (!ok) break;
+                const int first_zero = kmax - j * kBN;
+                uint8_t *vt = smem + OFF_V + st * kTileBytes;
+                for (int idx = lane; idx < (kBN - first_zero) * 16; idx += 32) {
+                    const int key = first_zero + idx / 16, half = (idx / 8) % 2, c = idx % 8;
+                    *reinterpret_cast<uint4 *>(vt + half * kHalf + key * 128 + c * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[V_ZERO]);
+            }
+        }
+        if (!ok && lane == 0) {  // let every copy already issued land
+            mbar_wait_drain(&bar[Q_FULL], 0);
+            for (int j = issued_k > kStages ? issued_k - kStages : 0; j < issued_k; ++j)
+                mbar_wait_drain(&bar[K_FULL + j % kStages], (j / kStages) & 1);
+            for (int j = issued_v > kStages ? issued_v - kStages : 0; j < issued_v; ++j)
+                mbar_wait_drain(&bar[V_FULL + j % kStages], (j / kStages) & 1);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -282,159 +377,193 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_s = instr_desc(E::kBf16, false, kBN);
             constexpr uint32_t idesc_pv = instr_desc(E::kBf16, true, kD);
             const uint32_t q_addr = smem_addr(smem + OFF_Q);
-            bool ok = mbar_wait(&bar[Q_FULL], 0, abort_flag, a.err);
-            int committed = 0;
+            const uint32_t k_addr = smem_addr(smem + OFF_K);
+            const uint32_t v_addr = smem_addr(smem + OFF_V);
+            // key tiles of query tile t: the last active tile needs nkt
+            int nkt_t[kTiles];
+            for (int t = 0; t < kTiles; ++t) {
+                const int rows_t = t < ntiles ? min(kBM, q_len - row0 - t * kBM) : 0;
+                const int kmax_t = ctx - q_len + row0 + t * kBM + rows_t;
+                nkt_t[t] = t < ntiles ? (kmax_t + kBN - 1) / kBN : 0;
+            }
+            auto issue_s = [&](int t, int st) {
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {  // S_t = Q_t K^T over the 128 dims
+                    const int half = ks / 4, kk = ks % 4;
+                    mma_ss(tmem + kTmemS + t * 128,
+                           smem_desc(q_addr + t * kTileBytes + half * kHalf + kk * 32, 16, 1024),
+                           smem_desc(k_addr + st * kTileBytes + half * kHalf + kk * 32, 16, 1024),
+                           idesc_s, ks > 0);
+                }
+            };
+            bool ok = mbar_wait(&bar[Q_FULL], 0, abort_flag, a.err) &&
+                      mbar_wait(&bar[K_FULL], 0, abort_flag, a.err);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < ntiles; ++t) {
+                    issue_s(t, 0);
+                    mma_commit(&bar[S_FULL + t]);
+                }
+                mma_commit(&bar[K_EMPTY]);
+            }
             for (int j = 0; j < nkt && ok; ++j) {
                 const int st = j % kStages;
-                ok = mbar_wait(&bar[K_FULL + st], (j / kStages) & 1, abort_flag, a.err);
-                if (ok && j > 0) ok = mbar_wait(&bar[S_EMPTY], (j - 1) & 1, abort_flag, a.err);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t k_addr = smem_addr(smem + OFF_K + st * kTileKV);
+                const int st1 = (j + 1) % kStages;
+                bool v_ready = false, k_next = false;
+                for (int t = 0; t < ntiles && ok; ++t) {
+                    if (j >= nkt_t[t]) continue;
+                    ok = mbar_wait(&bar[P_FULL + t], j & 1, abort_flag, a.err);
+                    if (ok && !v_ready) {
+                        ok = j == nkt - 1 ? mbar_wait(&bar[V_ZERO], 0, abort_flag, a.err)
+                                          : mbar_wait(&bar[V_FULL + st], (j / kStages) & 1,
+                                                      abort_flag, a.err);
+                        v_ready = true;
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {  // S = Q K^T over the 128 dims
-                    const int half = ks / 4, kk = ks % 4;
-                    mma_f16(tmem + kTmemS,
-                            smem_desc(q_addr + half * kHalfRowsQ + kk * 32, 16, 1024),
-                            smem_desc(k_addr + half * (kBN * 128) + kk * 32, 16, 1024), idesc_s,
-                            ks > 0);
+                    for (int pass = 0; pass < 2; ++pass)  // O_t += P_hi V + P_lo V
+#pragma unroll
+                        for (int ks = 0; ks < kBN / 16; ++ks)
+                            mma_ts(tmem + kTmemO + t * 128, tmem + kTmemS + t * 128 + pass * 64 + ks * 8,
+                                   smem_desc(v_addr + st * kTileBytes + ks * 2048, kHalf, 1024),
+                                   idesc_pv, j > 0 || pass > 0 || ks > 0);
+                    if (j + 1 < nkt_t[t]) {
+                        if (!k_next) {
+                            ok = mbar_wait(&bar[K_FULL + st1], ((j + 1) / kStages) & 1, abort_flag,
+                                           a.err);
+                            k_next = true;
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        issue_s(t, st1);
+                        mma_commit(&bar[S_FULL + t]);
+                    } else {
+                        mma_commit(&bar[O_FULL + t]);
+                    }
                 }
-                mma_commit(&bar[S_FULL]);
-                ok = mbar_wait(&bar[P_FULL], j & 1, abort_flag, a.err);
                 if (!ok) break;
-                tc_fence_after();
-                const uint32_t v_addr = smem_addr(smem + OFF_V + st * kTileKV);
-#pragma unroll
-                for (int pass = 0; pass < 2; ++pass) {  // PV = P_hi V + P_lo V
-                    const uint32_t p_addr = smem_addr(smem + (pass ? OFF_PLO : OFF_PHI));
-#pragma unroll
-                    for (int ks = 0; ks < kBN / 16; ++ks)
-                        mma_f16(tmem + kTmemPV, smem_desc(p_addr + ks * 32, 16, 1024),
-                                smem_desc(v_addr + ks * 2048, kBN * 128, 1024), idesc_pv,
-                                pass > 0 || ks > 0);
-                }
-                mma_commit(&bar[PV_FULL]);
-                mma_commit(&bar[KV_EMPTY + st]);
-                ++committed;
+                mma_commit(&bar[V_EMPTY + st]);
+                if (k_next) mma_commit(&bar[K_EMPTY + st1]);
             }
             // make sure no MMA is still running when the CTA releases TMEM
             mma_commit(&bar[MMA_DONE]);
             mbar_wait_drain(&bar[MMA_DONE], 0);
-            (void)committed;
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int r = threadIdx.x;                 // query row of this thread
-        const bool row_valid = r < rows;
-        const int pos = first_pos + r;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        float run_max = -INFINITY, run_sum = 0.f, alpha_prev = 0.f;
-        float o[kD];
-#pragma unroll
-        for (int d = 0; d < kD; ++d) o[d] = 0.f;
-        bool ok = true;
-        uint8_t *phi = smem + OFF_PHI + r * 128;
-        uint8_t *plo = smem + OFF_PLO + r * 128;
-        for (int j = 0; j < nkt && ok; ++j) {
-            const int st = j % kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar[S_FULL], j & 1, abort_flag, a.err));
-            if (!ok) break;
-            tc_fence_after();
-            float sc[kBN];
-            tmem_ld32(lane_base + kTmemS, *reinterpret_cast<float(*)[32]>(&sc[0]));
-            tmem_ld32(lane_base + kTmemS + 32, *reinterpret_cast<float(*)[32]>(&sc[32]));
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[S_EMPTY]);
-            // causal + context mask, scale into the log2 domain, online softmax
-            float tile_max = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                const int key = j * kBN + c;
-                sc[c] = (row_valid && key <= pos) ? sc[c] * a.scale_log2 : -INFINITY;
-                tile_max = fmaxf(tile_max, sc[c]);
-            }
-            const float new_max = fmaxf(run_max, tile_max);
-            const float ref = new_max == -INFINITY ? 0.f : new_max;
-            const float alpha = exp2f(run_max - ref);
-            float psum = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                sc[c] = exp2f(sc[c] - ref);
-                psum += sc[c];
-            }
-            run_sum = run_sum * alpha + psum;
-            run_max = new_max;
-            // fold in the previous tile's P V (its weights used the previous max)
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bar[PV_FULL], (j - 1) & 1, abort_flag, a.err));
+        const int t = warp / 4;                      // query tile of this warpgroup
+        const int r = (warp % 4) * 32 + lane;        // row within the tile = TMEM lane
+        if (t < ntiles) {
+            const int rows_t = min(kBM, q_len - row0 - t * kBM);
+            const int first_pos = ctx - q_len + row0 + t * kBM;
+            const int kmax_t = first_pos + rows_t;
+            const int my_nkt = (kmax_t + kBN - 1) / kBN;
+            const int pos = r < rows_t ? first_pos + r : -1;   // -1: padding row, all masked
+            const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+            const uint32_t s_col = lane_base + kTmemS + t * 128;
+            const uint32_t o_col = lane_base + kTmemO + t * 128;
+            const float c = a.scale_log2;
+            const bool scale_pos = c > 0.f;
+            const float cm = scale_pos ? c : 1.f;   // multiplier left for the exponent
+            float m_used = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < my_nkt && ok; ++j) {
+                ok = warp_all(mbar_wait(&bar[S_FULL + t], j & 1, abort_flag, a.err));
                 if (!ok) break;
                 tc_fence_after();
+                float x[kBN];
+                {
+                    uint32_t u[kBN];
 #pragma unroll
-                for (int c0 = 0; c0 < kD; c0 += 32) {
-                    float pv[32];
-                    tmem_ld32(lane_base + kTmemPV + c0, pv);
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        tmem_ld32_nowait(s_col + q4 * 32,
+                                         *reinterpret_cast<uint32_t(*)[32]>(&u[q4 * 32]));
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], alpha_prev, pv[i]);
+                    for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(u[i]);
                 }
-            }
-            alpha_prev = alpha;
-            // P = P_hi + P_lo as two 16-bit K-major rows (128-byte swizzle)
+                // scores into the log2 domain: for a positive scale the max of
+                // the raw scores is scaled once and the scale is folded into
+                // the exponent's FMA; otherwise every score is scaled first
+                if (!scale_pos) {
 #pragma unroll
-            for (int c8 = 0; c8 < kBN / 8; ++c8) {
-                uint16_t hi[8], lo[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float p = sc[c8 * 8 + e];
-                    hi[e] = E::round(p);
-                    lo[e] = E::round(p - E::widen(hi[e]));
+                    for (int i = 0; i < kBN; ++i) x[i] *= c;
                 }
-                const int chunk = (c8 ^ (r & 7)) * 16;
-                *reinterpret_cast<uint4 *>(phi + chunk) = *reinterpret_cast<const uint4 *>(hi);
-                *reinterpret_cast<uint4 *>(plo + chunk) = *reinterpret_cast<const uint4 *>(lo);
-            }
-            // V must have landed; past the last key its rows are zeroed
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bar[V_FULL + st], (j / kStages) & 1, abort_flag, a.err));
-            if (!ok) break;
-            if (j == nkt - 1) {
-                const int first_zero = kmax - j * kBN;       // tile-local key
-                const int nzero = kBN - first_zero;          // rows to clear
-                uint8_t *vt = smem + OFF_V + st * kTileKV;
-                for (int idx = threadIdx.x; idx < nzero * 2 * 8; idx += 128) {
-                    const int key = first_zero + idx / 16;
-                    const int half = (idx / 8) % 2, chunk = idx % 8;
-                    *reinterpret_cast<uint4 *>(vt + half * (kBN * 128) + (key / 8) * 1024 +
-                                               (key % 8) * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+                // causal mask (key j*128 + i visible to this row iff <= pos)
+                if (j * kBN + kBN - 1 > warp_min_pos) {
+                    const int lim = pos - j * kBN;
+#pragma unroll
+                    for (int i = 0; i < kBN; ++i) x[i] = i <= lim ? x[i] : -INFINITY;
                 }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < kBN; ++i) mx[i % 4] = fmaxf(mx[i % 4], x[i]);
+                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cm;
+                float m_new = m_used;
+                if (m_tile > m_used + kRescaleLog2) m_new = m_tile;
+                const float alpha = m_new == m_used ? 1.f : fast_exp2(m_used - m_new);
+                const float bias = m_new == -INFINITY ? 0.f : kBiasLog2 - m_new;
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < kBN; ++i) {
+                    x[i] = fast_exp2(fmaf(x[i], cm, bias));
+                    sum[i % 4] += x[i];
+                }
+                l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+                m_used = m_new;
+                // P_t into the S_t columns: P_hi at +0..63, P_lo at +64..127
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        E::split2(x[q4 * 32 + 2 * e], x[q4 * 32 + 2 * e + 1], hi[e], lo[e]);
+                    tmem_st16(s_col + q4 * 16, hi);
+                    tmem_st16(s_col + 64 + q4 * 16, lo);
+                }
+                // a raised maximum rescales O_t (its last update, P V of the
+                // previous tile, completed before this tile's S was signalled)
+                if (j > 0 && !warp_all(alpha == 1.f)) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t ov[32];
+                        tmem_ld32_nowait(o_col + q4 * 32, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(o_col + q4 * 32, ov);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[P_FULL + t]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_fence_before();
-            mbar_arrive(&bar[P_FULL]);
-        }
-        if (ok)
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bar[PV_FULL], (nkt - 1) & 1, abort_flag, a.err));
-        if (ok) {
-            tc_fence_after();
+            if (ok) ok = warp_all(mbar_wait(&bar[O_FULL + t], 0, abort_flag, a.err));
+            if (ok) {
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint16_t *dst = a.out + (static_cast<size_t>(q_first + row0 + t * kBM + r) * H + h) * kD;
 #pragma unroll
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                float pv[32];
-                tmem_ld32(lane_base + kTmemPV + c0, pv);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t ov[32];
+                    tmem_ld32_nowait(o_col + q4 * 32, ov);
+                    tmem_ld_wait();
+                    if (r < rows_t) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], alpha_prev, pv[i]);
-            }
-            if (row_valid) {
-                const float inv = run_sum > 0.f ? 1.f / run_sum : 0.f;
-                uint16_t *dst = a.out + (static_cast<size_t>(q_first + row0 + r) * H + h) * kD;
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            uint16_t v[8];
 #pragma unroll
-                for (int c8 = 0; c8 < kD / 8; ++c8) {
-                    uint16_t v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = E::round(o[c8 * 8 + e] * inv);
-                    *reinterpret_cast<uint4 *>(dst + c8 * 8) = *reinterpret_cast<const uint4 *>(v);
+                            for (int e = 0; e < 8; ++e)
+                                v[e] = E::round(__uint_as_float(ov[c8 * 8 + e]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + q4 * 32 + c8 * 8) =
+                                *reinterpret_cast<const uint4 *>(v);
+                        }
+                    }
                 }
             }
         }
@@ -525,8 +654,10 @@ cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((max_query_len + kBM - 1) / kBM),
-                       static_cast<unsigned>(H), static_cast<unsigned>(args.num_seqs));
+    const int pairs = (max_query_len + kTiles * kBM - 1) / (kTiles * kBM);
+    if (pairs > 65535) return cudaErrorInvalidValue;
+    cfg.gridDim = dim3(static_cast<unsigned>(H), static_cast<unsigned>(args.num_seqs),
+                       static_cast<unsigned>(pairs));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

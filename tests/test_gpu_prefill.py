@@ -77,3 +77,30 @@ def test_prefill_bad_query_count_is_reported(dev):
     ref = oracle.prefill(case.q[:40], case.k_cache, case.v_cache, case.block_tables[:1],
                          case.context_lens[:1], case.query_start[:2], case.scale)
     assert_parity(got[:40], ref, "the valid sequence is still computed")
+
+
+def _set_rising_scores(case, slope, q0):
+    """Scores that grow with the key's position: K[t, 0] = slope * t and
+    q[:, 0] = q0, so each row's running maximum rises tile after tile and the
+    kernel must rescale its accumulated output several times."""
+    bf16 = case.dtype == "bf16"
+    enc = (lambda v: workloads.f32_to_bf16_bits(np.asarray(v, np.float32))) if bf16 else \
+        (lambda v: np.asarray(v, np.float16))
+    B = case.k_cache.shape[2]
+    for s, ctx in enumerate(case.context_lens):
+        for t in range(int(ctx)):
+            case.k_cache[case.block_tables[s, t // B], :, t % B, 0] = enc(slope * t)
+    case.q[:, :, 0] = enc(q0)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_rising_maximum(dev, dtype):
+    ctx = np.array([513, 300, 129, 1000])
+    case = workloads.build_prefill_case("pf_rising", ctx, np.minimum(ctx, [513, 300, 129, 600]),
+                                        num_heads=2, head_dim=128, seed=47, dtype=dtype)
+    _set_rising_scores(case, 0.2, 4.0)
+    got, flags = run_prefill(case, dev)
+    assert flags == 0
+    ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
+                         case.context_lens, case.query_start, case.scale, dtype=dtype)
+    assert_parity(got, ref, f"prefill rising {dtype}", dtype=dtype)

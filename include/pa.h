@@ -196,21 +196,43 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  *                 q_len_s = query_start[s + 1] - query_start[s] tokens of its
  *                 context (a whole prompt, or its latest chunk)
  *   total_query_tokens  host: rows of q and out
- *   max_query_len host: an upper bound of every q_len_s (sizes the grid)
+ *   max_query_len host: an upper bound of every q_len_s (sizes the work)
  *   scale, max_blocks_per_seq, dims, stream: as pa_decode
  *
  * Query i of sequence s sits at position p = ctx_s - q_len_s + i and
  * attends to keys 0 .. p.  Built for head_dim 128, block_size 16, fp16 or
  * bf16 (PA_ERR_UNSUPPORTED otherwise).  Scores and softmax are fp32; the
  * probabilities enter the P V product as a pair of 16-bit values (P_hi +
- * P_lo) so the product keeps about 22 bits.  A sequence with q_len_s >
+ * P_lo) so the product keeps about 21 bits.  A sequence with q_len_s >
  * ctx_s, ctx_s > max_blocks_per_seq * B, or rows outside
  * [0, total_query_tokens) is skipped and flags PA_DEVERR_CONTEXT.
+ *
+ * The kernel is persistent (one CTA per SM) and takes its work items from a
+ * queue in two device counters; pa_prefill allocates them stream-ordered
+ * (cudaMallocAsync) for each call.  PA_ERR_SHAPE if ceil(max_query_len / 256)
+ * * S * H exceeds INT32_MAX.
  */
 int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                const int32_t *block_tables, const int32_t *context_lens,
                const int32_t *query_start, int32_t total_query_tokens, int32_t max_query_len,
                float scale, int32_t max_blocks_per_seq, const pa_dims *dims, void *stream);
+
+/* Bytes of the counters pa_prefill_ws takes. */
+#define PA_PREFILL_COUNTERS_BYTES 8
+
+/*
+ * pa_prefill_ws -- pa_prefill with caller-owned work-queue counters and no
+ * allocation.  counters: device, PA_PREFILL_COUNTERS_BYTES bytes (at least),
+ * 4-byte aligned, all zero on entry; the kernel leaves them zero on exit, so
+ * one buffer serves every call on one stream.  Two launches that run at the
+ * same time (different streams) must not share it.  PA_ERR_WORKSPACE if
+ * counters_bytes is too small.
+ */
+int pa_prefill_ws(void *out, const void *q, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, const int32_t *context_lens,
+                  const int32_t *query_start, int32_t total_query_tokens, int32_t max_query_len,
+                  float scale, int32_t max_blocks_per_seq, const pa_dims *dims,
+                  uint32_t *counters, size_t counters_bytes, void *stream);
 
 /*
  * Bytes of partial-result workspace pa_decode_ws needs for these sizes and

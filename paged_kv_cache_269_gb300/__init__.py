@@ -35,7 +35,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_UNSUPPO
           -7: "PA_ERR_OUT_OF_BLOCKS"}
 
 # Every symbol include/pa.h declares.
-EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill",
+EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", "pa_prefill_ws",
            "pa_decode_workspace_bytes",
            "pa_decode_counters_bytes", "pa_decode_ws", "pa_decode_static", "pa_device_errors",
            "pa_status_string", "pa_last_cuda_error", "pa_version",
@@ -72,6 +72,8 @@ def _declare(l):
     l.pa_copy_blocks.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, dp, vp]
     l.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp]
     l.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, dp, vp]
+    l.pa_prefill_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, dp, vp,
+                                ctypes.c_size_t, vp]
     l.pa_decode_workspace_bytes.argtypes = [dp, i32, i32]
     l.pa_decode_workspace_bytes.restype = sz
     l.pa_decode_counters_bytes.argtypes = [dp]
@@ -103,7 +105,8 @@ def _declare(l):
                  "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free", "pa_kvm_context_len",
                  "pa_kvm_slot", "pa_kvm_block_tables"):
         getattr(l, name).restype = i32
-    for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", "pa_decode_ws",
+    for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", "pa_prefill_ws",
+                 "pa_decode_ws",
                  "pa_device_errors",
                  "pa_last_cuda_error", "pa_version"):
         getattr(l, name).restype = ctypes.c_int
@@ -244,12 +247,18 @@ def copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
     _check(rc, "pa_copy_blocks")
 
 
+PREFILL_COUNTERS_BYTES = 8
+
+
 def prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
-            max_query_len=None, stream=None):
+            max_query_len=None, stream=None, counters=None, allocate_in_library=False):
     """Causal attention of the last q_len_s tokens of each sequence over its
-    paged K/V (pa_prefill).  q, out [total_q, H, D]; query_start [S + 1]
-    int32 on the device; max_query_len bounds every q_len_s (computed from
-    query_start, with a device sync, when None)."""
+    paged K/V (pa_prefill_ws; pa_prefill with allocate_in_library).  q, out
+    [total_q, H, D]; query_start [S + 1] int32 on the device; max_query_len
+    bounds every q_len_s (computed from query_start, with a device sync, when
+    None).  counters: a zeroed int32 CUDA tensor of at least 2 elements for
+    the kernel's work queue (left zeroed); by default one cached per (device,
+    stream)."""
     torch = _torch()
     _element_dtype(k_cache)
     et = k_cache.dtype
@@ -269,13 +278,39 @@ def prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start, s
     if max_query_len is None:
         max_query_len = int((query_start[1:] - query_start[:-1]).max()) if S else 0
     dims = _cache_dims(k_cache, S)
-    sh, _ = _stream_handle(dev, stream)
+    sh, st = _stream_handle(dev, stream)
     with torch.cuda.device(dev):
-        rc = lib().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                              _ptr(context_lens), _ptr(query_start), q.shape[0], int(max_query_len),
-                              float(scale), block_tables.shape[1], ctypes.byref(dims), sh)
+        if allocate_in_library:
+            rc = lib().pa_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(block_tables), _ptr(context_lens), _ptr(query_start),
+                                  q.shape[0], int(max_query_len), float(scale),
+                                  block_tables.shape[1], ctypes.byref(dims), sh)
+        else:
+            if counters is None:
+                counters = _prefill_counters_for(dev, st)
+            _need(counters, "counters", torch.int32, 1, dev)
+            rc = lib().pa_prefill_ws(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(block_tables), _ptr(context_lens), _ptr(query_start),
+                                     q.shape[0], int(max_query_len), float(scale),
+                                     block_tables.shape[1], ctypes.byref(dims), _ptr(counters),
+                                     counters.numel() * 4, sh)
     _check(rc, "pa_prefill")
     return out
+
+
+_prefill_counters = {}
+
+
+def _prefill_counters_for(device, stream):
+    torch = _torch()
+    key = (device.index, stream.cuda_stream)
+    with _buf_lock:
+        ctr = _prefill_counters.get(key)
+        if ctr is None:
+            with torch.cuda.stream(stream):
+                ctr = torch.zeros(16, dtype=torch.int32, device=device)
+            _prefill_counters[key] = ctr
+        return ctr
 
 
 def decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, num_blocks,
@@ -323,6 +358,8 @@ def reset_workspaces():
     """Zero every cached counter buffer (needed after a device error)."""
     with _buf_lock:
         for ctr, _ in _buffers.values():
+            ctr.zero_()
+        for ctr in _prefill_counters.values():
             ctr.zero_()
 
 

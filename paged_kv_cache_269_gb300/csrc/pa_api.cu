@@ -210,24 +210,29 @@ int pa_copy_blocks(const void *src_k, const void *src_v, int32_t src_num_blocks,
     return e == cudaSuccess ? PA_OK : fail_cuda(e);
 }
 
-int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
-               const int32_t *block_tables, const int32_t *context_lens,
-               const int32_t *query_start, int32_t total_query_tokens, int32_t max_query_len,
-               float scale, int32_t max_blocks_per_seq, const pa_dims *dims, void *stream) {
+int pa_prefill_ws(void *out, const void *q, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, const int32_t *context_lens,
+                  const int32_t *query_start, int32_t total_query_tokens, int32_t max_query_len,
+                  float scale, int32_t max_blocks_per_seq, const pa_dims *dims,
+                  uint32_t *counters, size_t counters_bytes, void *stream) {
     int rc = check_dims(dims, true);
     if (rc != PA_OK) return rc;
     if (!prefill_supported(dims->dtype, dims->head_dim, dims->block_size)) return PA_ERR_UNSUPPORTED;
     if (total_query_tokens < 0 || max_query_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
     if (dims->num_seqs == 0 || total_query_tokens == 0 || max_query_len == 0) return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start ||
+        !counters)
         return PA_ERR_NULL;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    if (counters_bytes < PA_PREFILL_COUNTERS_BYTES) return PA_ERR_WORKSPACE;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(counters, 4))
         return PA_ERR_ALIGN;
     if (!isfinite(scale)) return PA_ERR_SHAPE;
     // tensor-map coordinates are 32-bit: every cache row and query row must fit
+    const long long pairs = (static_cast<long long>(max_query_len) + 255) / 256;
     if (static_cast<long long>(dims->num_blocks) * dims->num_heads * dims->block_size > 0x7fffffffLL ||
         static_cast<long long>(max_blocks_per_seq) * dims->block_size > 0x7fffffffLL ||
-        dims->num_heads > 65535 || dims->num_seqs > 65535)
+        pairs * dims->num_seqs * dims->num_heads > 0x7fffffffLL)
         return PA_ERR_SHAPE;
     unsigned int *err = nullptr;
     int sms = 0;
@@ -244,10 +249,38 @@ int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cach
     a.num_blocks = dims->num_blocks;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.total_q = total_query_tokens;
+    a.num_pairs = static_cast<int32_t>(pairs);
+    a.counters = counters;
     a.err = err;
-    const cudaError_t e = launch_prefill(a, q, k_cache, v_cache, dims->dtype, max_query_len,
+    const cudaError_t e = launch_prefill(a, q, k_cache, v_cache, dims->dtype, sms,
                                          static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;  // tensor maps could not be made
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+int pa_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+               const int32_t *block_tables, const int32_t *context_lens,
+               const int32_t *query_start, int32_t total_query_tokens, int32_t max_query_len,
+               float scale, int32_t max_blocks_per_seq, const pa_dims *dims, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != PA_OK) return rc;
+    if (!prefill_supported(dims->dtype, dims->head_dim, dims->block_size)) return PA_ERR_UNSUPPORTED;
+    if (total_query_tokens < 0 || max_query_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+    if (dims->num_seqs == 0 || total_query_tokens == 0 || max_query_len == 0) return PA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *buf = nullptr;
+    cudaError_t e = cudaMallocAsync(&buf, PA_PREFILL_COUNTERS_BYTES, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = cudaMemsetAsync(buf, 0, PA_PREFILL_COUNTERS_BYTES, s);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(buf, s);
+        return fail_cuda(e);
+    }
+    rc = pa_prefill_ws(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                       total_query_tokens, max_query_len, scale, max_blocks_per_seq, dims,
+                       static_cast<uint32_t *>(buf), PA_PREFILL_COUNTERS_BYTES, stream);
+    e = cudaFreeAsync(buf, s);
+    if (rc != PA_OK) return rc;
     return e == cudaSuccess ? PA_OK : fail_cuda(e);
 }
 

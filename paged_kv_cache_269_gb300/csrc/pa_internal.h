@@ -63,13 +63,14 @@ struct PrefillArgs {
     int32_t num_blocks;
     int32_t max_blocks_per_seq;
     int32_t total_q;
+    int32_t num_pairs;             // ceil(max_query_len / 256): pairs of 128-row tiles
+    uint32_t *counters;            // [2]: next work item, CTAs done; zero on entry and exit
     unsigned int *err;
 };
 
 bool prefill_supported(int dtype, int head_dim, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k_cache,
-                           const void *v_cache, int dtype, int max_query_len,
-                           cudaStream_t stream);
+                           const void *v_cache, int dtype, int num_sms, cudaStream_t stream);
 
 // SM count and device error word of the current device (set up on first use).
 int current_device_info(unsigned int **err, int *num_sms);

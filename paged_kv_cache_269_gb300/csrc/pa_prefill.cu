@@ -60,9 +60,24 @@ constexpr int kBN = 128;            // keys per tile
 constexpr int kB = 16;              // block_size
 constexpr int kBlocksPerTile = kBN / kB;
 constexpr int kStages = 2;
-constexpr int kThreads = 320;       // 2 x 4 softmax warps + TMA warp + MMA warp
+constexpr int kThreads = 384;       // 2 x 4 softmax warps; TMA warp, 2 MMA warps, 1 idle warp
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp0 = 9;        // issues query tile 0's products; warp 10 tile 1's
+// Register split: launched at 168 per thread (384 threads), the third
+// warpgroup (TMA, MMA, idle) gives registers up to the two softmax
+// warpgroups; the three shares must fit the block's launch allotment of
+// 3 x 168 per lane.
+#ifndef PA_PREFILL_REGS_SOFTMAX
+#define PA_PREFILL_REGS_SOFTMAX 208
+#endif
+#ifndef PA_PREFILL_REGS_OTHER
+#define PA_PREFILL_REGS_OTHER 88
+#endif
+constexpr int kRegsSoftmax = PA_PREFILL_REGS_SOFTMAX;
+constexpr int kRegsOther = PA_PREFILL_REGS_OTHER;
+static_assert(2 * kRegsSoftmax + kRegsOther <= 3 * 168, "register split exceeds the launch");
+static_assert(kRegsSoftmax % 8 == 0 && kRegsOther % 8 == 0 && kRegsOther >= 24, "bad split");
+
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;      // S_t / P_t: columns 128 t .. 128 t + 127
 constexpr uint32_t kTmemO = 256;    // O_t: columns 256 + 128 t .. 256 + 128 t + 127
@@ -82,16 +97,24 @@ enum Bar {
     K_EMPTY = 3,         // [stage]
     V_FULL = 5,          // [stage]
     V_EMPTY = 7,         // [stage]
-    V_ZERO = 9,          // last V tile loaded and its tail rows cleared
+    V_ZERO = 9,          // an item's last V tile loaded and its tail rows cleared
     S_FULL = 10,         // [tile]
     P_FULL = 12,         // [tile], one arrival per softmax warp
     O_FULL = 14,         // [tile]
-    MMA_DONE = 16,
-    kNumBars = 17
+    MMA_DONE = 16,       // [tile]
+    Q_EMPTY = 18,        // every S product of the item complete (one arrival per MMA thread)
+    O_EMPTY = 19,        // [tile], the epilogue has read O_t
+    ITEM_FULL = 21,      // [slot] of the work-item ring
+    ITEM_EMPTY = 23,     // [slot]
+    kNumBars = 25
 };
+// K_EMPTY, V_EMPTY and Q_EMPTY take one arrival from each MMA thread; a
+// thread arrives on an EMPTY barrier only after waiting for the matching
+// FULL phase, so an arrival can never count toward an earlier phase.
 constexpr int OFF_TMEM = OFF_BAR + kNumBars * 8;
 constexpr int OFF_FLAG = OFF_TMEM + 8;
-constexpr int kSmemBytes = OFF_FLAG + 8 + 1024;  // + alignment slack
+constexpr int OFF_ITEM = OFF_FLAG + 8;              // int[2]
+constexpr int kSmemBytes = OFF_ITEM + 8 + 1024;  // + alignment slack
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
@@ -194,6 +217,36 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed fp32 pair arithmetic (one instruction for two lanes of data).
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max of three
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y,
                                             uint64_t *bar) {
     asm volatile(
@@ -221,8 +274,10 @@ struct F16T {
     __device__ static __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
         const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
         const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+        float l0, l1;
+        sub2(l0, l1, p0, p1, h0, h1);
         const __half2 h = __floats2half2_rn(h0, h1);
-        const __half2 l = __floats2half2_rn(p0 - h0, p1 - h1);
+        const __half2 l = __floats2half2_rn(l0, l1);
         hi = *reinterpret_cast<const uint32_t *>(&h);
         lo = *reinterpret_cast<const uint32_t *>(&l);
     }
@@ -236,8 +291,9 @@ struct BF16T {
     __device__ static __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
         const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
         hi = __byte_perm(b0, b1, 0x7632);   // upper halves: the truncated bf16 values
-        const __nv_bfloat162 l = __floats2bfloat162_rn(p0 - __uint_as_float(b0 & 0xFFFF0000u),
-                                                       p1 - __uint_as_float(b1 & 0xFFFF0000u));
+        float l0, l1;
+        sub2(l0, l1, p0, p1, __uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u));
+        const __nv_bfloat162 l = __floats2bfloat162_rn(l0, l1);
         lo = *reinterpret_cast<const uint32_t *>(&l);
     }
     __device__ static __forceinline__ uint16_t round(float x) {
@@ -247,6 +303,45 @@ struct BF16T {
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+// One work item: a pair of query tiles of one (sequence, head).
+struct Item {
+    int s, h, row0, q_first, q_len, ctx, ntiles, kmax, nkt;
+};
+
+// Work item w, heaviest pairs (latest positions) first: w = (level, s, h)
+// with pair = num_pairs - 1 - level.  Returns false for an empty item (the
+// sequence has no query rows in that pair) or, with `check`, for a sequence
+// whose lengths are inconsistent (recorded in the error word).
+__device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool check, Item &it) {
+    const int sh = a.num_seqs * a.num_heads;
+    const int level = w / sh;
+    const int rem = w - level * sh;
+    it.s = rem / a.num_heads;
+    it.h = rem - it.s * a.num_heads;
+    const int pair = a.num_pairs - 1 - level;
+    it.q_first = __ldg(a.query_start + it.s);
+    it.q_len = __ldg(a.query_start + it.s + 1) - it.q_first;
+    it.ctx = __ldg(a.context_lens + it.s);
+    it.row0 = pair * kTiles * kBM;
+    if (it.q_len <= 0 || it.row0 >= it.q_len) return false;
+    if (it.ctx > a.max_blocks_per_seq * kB || it.q_len > it.ctx || it.q_first < 0 ||
+        it.q_first + it.q_len > a.total_q) {
+        if (check && it.h == 0 && it.row0 == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
+        return false;
+    }
+    it.ntiles = it.q_len - it.row0 > kBM ? 2 : 1;
+    const int rows_last = min(kBM, it.q_len - it.row0 - (it.ntiles - 1) * kBM);
+    it.kmax = it.ctx - it.q_len + it.row0 + (it.ntiles - 1) * kBM + rows_last;
+    it.nkt = (it.kmax + kBN - 1) / kBN;
+    return true;
+}
+
+// key tiles needed by query tile t of an item
+__device__ __forceinline__ int tile_key_tiles(const Item &it, int t) {
+    const int rows_t = min(kBM, it.q_len - it.row0 - t * kBM);
+    return (it.ctx - it.q_len + it.row0 + t * kBM + rows_t + kBN - 1) / kBN;
+}
 
 template <typename E>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -258,33 +353,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
+    volatile int *item_ring = reinterpret_cast<volatile int *>(smem + OFF_ITEM);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // heaviest pairs (latest positions, most keys) are scheduled first
-    const int h = blockIdx.x, s = blockIdx.y, pair = gridDim.z - 1 - blockIdx.z;
     const int H = a.num_heads;
-
-    grid_dependency_wait();
-    allow_dependents_to_launch();
-    const int q_first = a.query_start[s];
-    const int q_len = a.query_start[s + 1] - q_first;
-    const int ctx = a.context_lens[s];
-    const int row0 = pair * kTiles * kBM;
-    if (q_len <= 0 || row0 >= q_len) return;  // nothing for this CTA (before any set-up)
-    if (ctx > a.max_blocks_per_seq * kB || q_len > ctx || q_first < 0 ||
-        q_first + q_len > a.total_q) {
-        if (threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
-        return;
-    }
-    const int ntiles = q_len - row0 > kBM ? 2 : 1;
-    // tile t: rows row0 + 128 t ..; the last active tile needs the most keys
-    const int rows_last = min(kBM, q_len - row0 - (ntiles - 1) * kBM);
-    const int kmax = ctx - q_len + row0 + (ntiles - 1) * kBM + rows_last;  // keys 0 .. kmax-1
-    const int nkt = (kmax + kBN - 1) / kBN;
-    const int nblk_needed = (kmax + kB - 1) / kB;
+    const int num_items = a.num_pairs * a.num_seqs * a.num_heads;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i)
-            mbar_init(&bar[i], (i == P_FULL || i == P_FULL + 1) ? 4 : 1);
+        for (int i = 0; i < kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == P_FULL || i == P_FULL + 1 || i == O_EMPTY || i == O_EMPTY + 1)
+                count = 4;                       // one arrival per softmax warp
+            else if (i == ITEM_EMPTY || i == ITEM_EMPTY + 1)
+                count = 10;                      // the 2 MMA threads and the 8 softmax warps
+            else if (i == K_EMPTY || i == K_EMPTY + 1 || i == V_EMPTY || i == V_EMPTY + 1 ||
+                     i == Q_EMPTY)
+                count = 2;                       // the 2 MMA threads
+            mbar_init(&bar[i], count);
+        }
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -298,180 +383,266 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // global memory written by the previous kernel on the stream is read only
+    // after this point
+    grid_dependency_wait();
+    allow_dependents_to_launch();
 
-    if (warp == kTmaWarp) {
+    if (warp >= 8) {
+      // the register split is made at the top of each warpgroup's branch, so
+      // the compiler allocates each role against its own limit
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+      if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA
-        int issued_k = 0, issued_v = 0;
+        // Takes items from the queue, publishes them to the other roles
+        // through a two-slot ring, and loads their Q, K and V.
+        uint32_t gk = 0, gv = 0;   // K / V tiles issued, over all items
+        int k = 0;           // items published
+        int q_loads = 0;     // Q loads issued
         bool ok = true;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bar[Q_FULL], ntiles * kTileBytes);
-            for (int t = 0; t < ntiles; ++t)
-                for (int half = 0; half < 2; ++half)
-                    tma_load_3d(smem + OFF_Q + t * kTileBytes + half * kHalf, &tm_q, half * 64, h,
-                                q_first + row0 + t * kBM, &bar[Q_FULL]);
-        }
-        const int32_t *table = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
-        for (int j = 0; j < nkt && ok; ++j) {
-            const int st = j % kStages;
-            const uint32_t ph = (j / kStages) & 1;
-            // physical blocks of this key tile: lane i < 8 looks up block i
-            int phys = -1;
-            const int b = j * kBlocksPerTile + lane;
-            if (lane < kBlocksPerTile && b < nblk_needed) {
-                const int p = __ldg(table + b);
-                if (static_cast<unsigned>(p) < static_cast<unsigned>(a.num_blocks))
-                    phys = p;
-                else
-                    atomicOr(a.err, PA_DEVERR_TABLE);
+        for (;;) {
+            int w = 0;
+            Item it;
+            for (;;) {       // next non-empty item, or the end of the queue
+                if (lane == 0) w = static_cast<int>(atomicAdd(a.counters, 1u));
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (w >= num_items) break;
+                if (item_geometry(a, w, lane == 0, it)) break;
             }
-            const unsigned valid_mask = __ballot_sync(0xffffffffu, phys >= 0);
-            const uint32_t bytes = __popc(valid_mask) * 2u * kB * 128u;
-            const int y = (phys * H + h) * kB;
-            ok = warp_all(mbar_wait(&bar[K_EMPTY + st], ph ^ 1, abort_flag, a.err));
+            const bool done = w >= num_items;
+            const int slot = k % 2;
+            ok = warp_all(mbar_wait(&bar[ITEM_EMPTY + slot], ((k / 2) & 1) ^ 1, abort_flag, a.err));
             if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&bar[K_FULL + st], bytes);
-            __syncwarp();
-            if (phys >= 0) {
-                uint8_t *dst = smem + OFF_K + st * kTileBytes + lane * (kB * 128);
-                tma_load_2d(dst, &tm_k, 0, y, &bar[K_FULL + st]);
-                tma_load_2d(dst + kHalf, &tm_k, 64, y, &bar[K_FULL + st]);
+            if (lane == 0) {
+                item_ring[slot] = done ? -1 : w;
+                mbar_arrive(&bar[ITEM_FULL + slot]);   // release: the slot is visible
             }
-            ++issued_k;
-            ok = warp_all(mbar_wait(&bar[V_EMPTY + st], ph ^ 1, abort_flag, a.err));
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&bar[V_FULL + st], bytes);
-            __syncwarp();
-            if (phys >= 0) {
-                uint8_t *dst = smem + OFF_V + st * kTileBytes + lane * (kB * 128);
-                tma_load_2d(dst, &tm_v, 0, y, &bar[V_FULL + st]);
-                tma_load_2d(dst + kHalf, &tm_v, 64, y, &bar[V_FULL + st]);
-            }
-            ++issued_v;
-            if (j == nkt - 1) {
-                // clear V rows kmax .. end of the tile once the loads have landed
-                ok = warp_all(mbar_wait(&bar[V_FULL + st], ph, abort_flag, a.err));
+            if (done) break;
+            // Q: the previous item's S products must all have been issued and done
+            if (k > 0) {
+                ok = warp_all(mbar_wait(&bar[Q_EMPTY], (k - 1) & 1, abort_flag, a.err));
                 if (!ok) break;
-                const int first_zero = kmax - j * kBN;
-                uint8_t *vt = smem + OFF_V + st * kTileBytes;
-                for (int idx = lane; idx < (kBN - first_zero) * 16; idx += 32) {
-                    const int key = first_zero + idx / 16, half = (idx / 8) % 2, c = idx % 8;
-                    *reinterpret_cast<uint4 *>(vt + half * kHalf + key * 128 + c * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[V_ZERO]);
             }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar[Q_FULL], it.ntiles * kTileBytes);
+                for (int t = 0; t < it.ntiles; ++t)
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_3d(smem + OFF_Q + t * kTileBytes + half * kHalf, &tm_q, half * 64,
+                                    it.h, it.q_first + it.row0 + t * kBM, &bar[Q_FULL]);
+            }
+            ++q_loads;
+            const int nblk_needed = (it.kmax + kB - 1) / kB;
+            const int32_t *table = a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq;
+            for (int j = 0; j < it.nkt && ok; ++j) {
+                const int st = gk % kStages;
+                const uint32_t ph = (gk / kStages) & 1;
+                // physical blocks of this key tile: lane i < 8 looks up block i
+                int phys = -1;
+                const int b = j * kBlocksPerTile + lane;
+                if (lane < kBlocksPerTile && b < nblk_needed) {
+                    const int p = __ldg(table + b);
+                    if (static_cast<unsigned>(p) < static_cast<unsigned>(a.num_blocks))
+                        phys = p;
+                    else
+                        atomicOr(a.err, PA_DEVERR_TABLE);
+                }
+                const unsigned valid_mask = __ballot_sync(0xffffffffu, phys >= 0);
+                const uint32_t bytes = __popc(valid_mask) * 2u * kB * 128u;
+                const int y = (phys * H + it.h) * kB;
+                ok = warp_all(mbar_wait(&bar[K_EMPTY + st], ph ^ 1, abort_flag, a.err));
+                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(&bar[K_FULL + st], bytes);
+                __syncwarp();
+                if (phys >= 0) {
+                    uint8_t *dst = smem + OFF_K + st * kTileBytes + lane * (kB * 128);
+                    tma_load_2d(dst, &tm_k, 0, y, &bar[K_FULL + st]);
+                    tma_load_2d(dst + kHalf, &tm_k, 64, y, &bar[K_FULL + st]);
+                }
+                ++gk;
+                ok = warp_all(mbar_wait(&bar[V_EMPTY + st], ph ^ 1, abort_flag, a.err));
+                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(&bar[V_FULL + st], bytes);
+                __syncwarp();
+                if (phys >= 0) {
+                    uint8_t *dst = smem + OFF_V + st * kTileBytes + lane * (kB * 128);
+                    tma_load_2d(dst, &tm_v, 0, y, &bar[V_FULL + st]);
+                    tma_load_2d(dst + kHalf, &tm_v, 64, y, &bar[V_FULL + st]);
+                }
+                ++gv;
+                if (j == it.nkt - 1) {
+                    // clear V rows kmax .. end of the tile once the loads have landed
+                    ok = warp_all(mbar_wait(&bar[V_FULL + st], ph, abort_flag, a.err));
+                    if (!ok) break;
+                    const int first_zero = it.kmax - j * kBN;
+                    uint8_t *vt = smem + OFF_V + st * kTileBytes;
+                    for (int idx = lane; idx < (kBN - first_zero) * 16; idx += 32) {
+                        const int key = first_zero + idx / 16, half = (idx / 8) % 2, c = idx % 8;
+                        *reinterpret_cast<uint4 *>(vt + half * kHalf + key * 128 + c * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[V_ZERO]);
+                }
+            }
+            if (!ok) break;
+            ++k;
         }
-        if (!ok && lane == 0) {  // let every copy already issued land
-            mbar_wait_drain(&bar[Q_FULL], 0);
-            for (int j = issued_k > kStages ? issued_k - kStages : 0; j < issued_k; ++j)
-                mbar_wait_drain(&bar[K_FULL + j % kStages], (j / kStages) & 1);
-            for (int j = issued_v > kStages ? issued_v - kStages : 0; j < issued_v; ++j)
-                mbar_wait_drain(&bar[V_FULL + j % kStages], (j / kStages) & 1);
+        if (lane == 0) {
+            if (!ok) {  // let every copy already issued land
+                if (q_loads > 0) mbar_wait_drain(&bar[Q_FULL], (q_loads - 1) & 1);
+                for (uint32_t i = gk > kStages ? gk - kStages : 0; i < gk; ++i)
+                    mbar_wait_drain(&bar[K_FULL + i % kStages], (i / kStages) & 1);
+                for (uint32_t i = gv > kStages ? gv - kStages : 0; i < gv; ++i)
+                    mbar_wait_drain(&bar[V_FULL + i % kStages], (i / kStages) & 1);
+            }
+            // the last CTA to leave the queue leaves both counters at zero for
+            // the next launch
+            __threadfence();
+            if (atomicAdd(a.counters + 1, 1u) == gridDim.x - 1) {
+                atomicExch(a.counters, 0u);
+                atomicExch(a.counters + 1, 0u);
+            }
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
+      } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
         // ------------------------------------------------------------ MMA
+        // One thread per query tile, so the two tiles' issue streams (and
+        // their waits) proceed independently; each thread's own products
+        // execute in issue order, which keeps S_t(j + 1) behind the P_t V
+        // product that reads the same tensor-memory columns.
         if (lane == 0) {
+            const int t = warp - kMmaWarp0;
             constexpr uint32_t idesc_s = instr_desc(E::kBf16, false, kBN);
             constexpr uint32_t idesc_pv = instr_desc(E::kBf16, true, kD);
-            const uint32_t q_addr = smem_addr(smem + OFF_Q);
+            const uint32_t q_addr = smem_addr(smem + OFF_Q) + t * kTileBytes;
             const uint32_t k_addr = smem_addr(smem + OFF_K);
             const uint32_t v_addr = smem_addr(smem + OFF_V);
-            // key tiles of query tile t: the last active tile needs nkt
-            int nkt_t[kTiles];
-            for (int t = 0; t < kTiles; ++t) {
-                const int rows_t = t < ntiles ? min(kBM, q_len - row0 - t * kBM) : 0;
-                const int kmax_t = ctx - q_len + row0 + t * kBM + rows_t;
-                nkt_t[t] = t < ntiles ? (kmax_t + kBN - 1) / kBN : 0;
-            }
-            auto issue_s = [&](int t, int st) {
+            const uint32_t tm_s = tmem + kTmemS + t * 128;
+            const uint32_t tm_o = tmem + kTmemO + t * 128;
+            auto issue_s = [&](int st) {
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {  // S_t = Q_t K^T over the 128 dims
                     const int half = ks / 4, kk = ks % 4;
-                    mma_ss(tmem + kTmemS + t * 128,
-                           smem_desc(q_addr + t * kTileBytes + half * kHalf + kk * 32, 16, 1024),
+                    mma_ss(tm_s, smem_desc(q_addr + half * kHalf + kk * 32, 16, 1024),
                            smem_desc(k_addr + st * kTileBytes + half * kHalf + kk * 32, 16, 1024),
                            idesc_s, ks > 0);
                 }
             };
-            bool ok = mbar_wait(&bar[Q_FULL], 0, abort_flag, a.err) &&
-                      mbar_wait(&bar[K_FULL], 0, abort_flag, a.err);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < ntiles; ++t) {
-                    issue_s(t, 0);
-                    mma_commit(&bar[S_FULL + t]);
-                }
-                mma_commit(&bar[K_EMPTY]);
-            }
-            for (int j = 0; j < nkt && ok; ++j) {
-                const int st = j % kStages;
-                const int st1 = (j + 1) % kStages;
-                bool v_ready = false, k_next = false;
-                for (int t = 0; t < ntiles && ok; ++t) {
-                    if (j >= nkt_t[t]) continue;
-                    ok = mbar_wait(&bar[P_FULL + t], j & 1, abort_flag, a.err);
-                    if (ok && !v_ready) {
-                        ok = j == nkt - 1 ? mbar_wait(&bar[V_ZERO], 0, abort_flag, a.err)
-                                          : mbar_wait(&bar[V_FULL + st], (j / kStages) & 1,
-                                                      abort_flag, a.err);
-                        v_ready = true;
-                    }
-                    if (!ok) break;
+            uint32_t g = 0;      // key tiles consumed, over all items
+            uint32_t pc = 0;     // P_FULL phases consumed
+            uint32_t oc = 0;     // items in which this query tile was active
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int slot = k % 2;
+                ok = mbar_wait(&bar[ITEM_FULL + slot], (k / 2) & 1, abort_flag, a.err);
+                if (!ok) break;
+                const int w = item_ring[slot];
+                mbar_arrive(&bar[ITEM_EMPTY + slot]);
+                if (w < 0) break;
+                Item it;
+                item_geometry(a, w, false, it);
+                const bool active = t < it.ntiles;
+                const int nk = active ? tile_key_tiles(it, t) : 0;
+                ok = mbar_wait(&bar[Q_FULL], k & 1, abort_flag, a.err) &&
+                     mbar_wait(&bar[K_FULL + g % kStages], (g / kStages) & 1, abort_flag, a.err);
+                if (!ok) break;
+                if (active) {
                     tc_fence_after();
+                    issue_s(g % kStages);
+                    mma_commit(&bar[S_FULL + t]);
+                    mma_commit(&bar[K_EMPTY + g % kStages]);
+                    if (nk == 1) mma_commit(&bar[Q_EMPTY]);
+                } else {
+                    mbar_arrive(&bar[K_EMPTY + g % kStages]);
+                    mbar_arrive(&bar[Q_EMPTY]);
+                }
+                for (int j = 0; j < it.nkt && ok; ++j, ++g) {
+                    const int st = g % kStages, st1 = (g + 1) % kStages;
+                    const bool last = j == it.nkt - 1;
+                    ok = last ? mbar_wait(&bar[V_ZERO], k & 1, abort_flag, a.err)
+                              : mbar_wait(&bar[V_FULL + st], (g / kStages) & 1, abort_flag, a.err);
+                    if (!ok) break;
+                    if (j < nk) {
+                        ok = mbar_wait(&bar[P_FULL + t], pc & 1, abort_flag, a.err);
+                        ++pc;
+                        // O_t still holds the previous item's result until its
+                        // epilogue has read it
+                        if (ok && j == 0 && oc > 0)
+                            ok = mbar_wait(&bar[O_EMPTY + t], (oc - 1) & 1, abort_flag, a.err);
+                        if (!ok) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int pass = 0; pass < 2; ++pass)  // O_t += P_hi V + P_lo V
+                        for (int pass = 0; pass < 2; ++pass)  // O_t += P_hi V + P_lo V
 #pragma unroll
-                        for (int ks = 0; ks < kBN / 16; ++ks)
-                            mma_ts(tmem + kTmemO + t * 128, tmem + kTmemS + t * 128 + pass * 64 + ks * 8,
-                                   smem_desc(v_addr + st * kTileBytes + ks * 2048, kHalf, 1024),
-                                   idesc_pv, j > 0 || pass > 0 || ks > 0);
-                    if (j + 1 < nkt_t[t]) {
-                        if (!k_next) {
-                            ok = mbar_wait(&bar[K_FULL + st1], ((j + 1) / kStages) & 1, abort_flag,
+                            for (int ks = 0; ks < kBN / 16; ++ks)
+                                mma_ts(tm_o, tm_s + pass * 64 + ks * 8,
+                                       smem_desc(v_addr + st * kTileBytes + ks * 2048, kHalf, 1024),
+                                       idesc_pv, j > 0 || pass > 0 || ks > 0);
+                        mma_commit(&bar[V_EMPTY + st]);
+                        if (j + 1 < nk) {
+                            ok = mbar_wait(&bar[K_FULL + st1], ((g + 1) / kStages) & 1, abort_flag,
                                            a.err);
-                            k_next = true;
                             if (!ok) break;
                             tc_fence_after();
+                            issue_s(st1);
+                            mma_commit(&bar[S_FULL + t]);
+                            mma_commit(&bar[K_EMPTY + st1]);
+                            if (j + 2 == nk) mma_commit(&bar[Q_EMPTY]);  // last S issued
+                            continue;
                         }
-                        issue_s(t, st1);
-                        mma_commit(&bar[S_FULL + t]);
-                    } else {
                         mma_commit(&bar[O_FULL + t]);
+                    } else {
+                        mbar_arrive(&bar[V_EMPTY + st]);
+                    }
+                    if (!last) {  // the next K tile is not used by this query tile
+                        ok = mbar_wait(&bar[K_FULL + st1], ((g + 1) / kStages) & 1, abort_flag, a.err);
+                        if (!ok) break;
+                        mbar_arrive(&bar[K_EMPTY + st1]);
                     }
                 }
-                if (!ok) break;
-                mma_commit(&bar[V_EMPTY + st]);
-                if (k_next) mma_commit(&bar[K_EMPTY + st1]);
+                if (active) ++oc;
             }
-            // make sure no MMA is still running when the CTA releases TMEM
-            mma_commit(&bar[MMA_DONE]);
-            mbar_wait_drain(&bar[MMA_DONE], 0);
+            // make sure none of this thread's products is still running when
+            // the CTA releases TMEM
+            mma_commit(&bar[MMA_DONE + t]);
+            mbar_wait_drain(&bar[MMA_DONE + t], 0);
         }
         __syncwarp();
+      }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ------------------------------------------------------------ softmax
         const int t = warp / 4;                      // query tile of this warpgroup
         const int r = (warp % 4) * 32 + lane;        // row within the tile = TMEM lane
-        if (t < ntiles) {
-            const int rows_t = min(kBM, q_len - row0 - t * kBM);
-            const int first_pos = ctx - q_len + row0 + t * kBM;
-            const int kmax_t = first_pos + rows_t;
-            const int my_nkt = (kmax_t + kBN - 1) / kBN;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+        const uint32_t s_col = lane_base + kTmemS + t * 128;
+        const uint32_t o_col = lane_base + kTmemO + t * 128;
+        const float c = a.scale_log2;
+        const bool scale_pos = c > 0.f;
+        const float cm = scale_pos ? c : 1.f;   // multiplier left for the exponent
+        uint32_t s_cnt = 0, o_cnt = 0;          // S_FULL / O_FULL phases consumed
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int slot = k % 2;
+            ok = warp_all(mbar_wait(&bar[ITEM_FULL + slot], (k / 2) & 1, abort_flag, a.err));
+            if (!ok) break;
+            const int w = item_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[ITEM_EMPTY + slot]);
+            if (w < 0) break;
+            Item it;
+            item_geometry(a, w, false, it);
+            if (t >= it.ntiles) continue;
+            const int rows_t = min(kBM, it.q_len - it.row0 - t * kBM);
+            const int first_pos = it.ctx - it.q_len + it.row0 + t * kBM;
+            const int my_nkt = (first_pos + rows_t + kBN - 1) / kBN;
             const int pos = r < rows_t ? first_pos + r : -1;   // -1: padding row, all masked
             const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-            const uint32_t s_col = lane_base + kTmemS + t * 128;
-            const uint32_t o_col = lane_base + kTmemO + t * 128;
-            const float c = a.scale_log2;
-            const bool scale_pos = c > 0.f;
-            const float cm = scale_pos ? c : 1.f;   // multiplier left for the exponent
             float m_used = -INFINITY, l = 0.f;
-            bool ok = true;
             for (int j = 0; j < my_nkt && ok; ++j) {
-                ok = warp_all(mbar_wait(&bar[S_FULL + t], j & 1, abort_flag, a.err));
+                ok = warp_all(mbar_wait(&bar[S_FULL + t], s_cnt & 1, abort_flag, a.err));
+                ++s_cnt;
                 if (!ok) break;
                 tc_fence_after();
                 float x[kBN];
@@ -500,19 +671,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) mx[i % 4] = fmaxf(mx[i % 4], x[i]);
-                const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cm;
+                for (int i = 0; i < kBN; i += 8)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) mx[q] = max3(mx[q], x[i + 2 * q], x[i + 2 * q + 1]);
+                const float m_tile = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * cm;
                 float m_new = m_used;
                 if (m_tile > m_used + kRescaleLog2) m_new = m_tile;
                 const float alpha = m_new == m_used ? 1.f : fast_exp2(m_used - m_new);
                 const float bias = m_new == -INFINITY ? 0.f : kBiasLog2 - m_new;
-                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) {
-                    x[i] = fast_exp2(fmaf(x[i], cm, bias));
-                    sum[i % 4] += x[i];
+                for (int i = 0; i < kBN; i += 8) {
+#pragma unroll
+                    for (int q = 0; q < 8; q += 2) {
+                        fma2(x[i + q], x[i + q + 1], x[i + q], x[i + q + 1], cm, cm, bias, bias);
+                        x[i + q] = fast_exp2(x[i + q]);
+                        x[i + q + 1] = fast_exp2(x[i + q + 1]);
+                        add2(sum[q], sum[q + 1], sum[q], sum[q + 1], x[i + q], x[i + q + 1]);
+                    }
                 }
-                l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+                add2(sum[0], sum[1], sum[0], sum[1], sum[2], sum[3]);
+                add2(sum[4], sum[5], sum[4], sum[5], sum[6], sum[7]);
+                add2(sum[0], sum[1], sum[0], sum[1], sum[4], sum[5]);
+                l = l * alpha + (sum[0] + sum[1]);
                 m_used = m_new;
                 // P_t into the S_t columns: P_hi at +0..63, P_lo at +64..127
 #pragma unroll
@@ -543,27 +724,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[P_FULL + t]);
             }
-            if (ok) ok = warp_all(mbar_wait(&bar[O_FULL + t], 0, abort_flag, a.err));
-            if (ok) {
-                tc_fence_after();
+            if (!ok) break;
+            // epilogue: read O_t, hand its columns back to the MMA warp, then
+            // normalise and store
+            ok = warp_all(mbar_wait(&bar[O_FULL + t], o_cnt & 1, abort_flag, a.err));
+            ++o_cnt;
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t ov[kD];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_ld32_nowait(o_col + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[q4 * 32]));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[O_EMPTY + t]);
+            if (r < rows_t) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint16_t *dst = a.out + (static_cast<size_t>(q_first + row0 + t * kBM + r) * H + h) * kD;
+                uint16_t *dst =
+                    a.out + (static_cast<size_t>(it.q_first + it.row0 + t * kBM + r) * H + it.h) * kD;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t ov[32];
-                    tmem_ld32_nowait(o_col + q4 * 32, ov);
-                    tmem_ld_wait();
-                    if (r < rows_t) {
+                for (int c8 = 0; c8 < kD / 8; ++c8) {
+                    uint16_t v[8];
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            uint16_t v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                v[e] = E::round(__uint_as_float(ov[c8 * 8 + e]) * inv);
-                            *reinterpret_cast<uint4 *>(dst + q4 * 32 + c8 * 8) =
-                                *reinterpret_cast<const uint4 *>(v);
-                        }
-                    }
+                    for (int e = 0; e < 8; ++e) v[e] = E::round(__uint_as_float(ov[c8 * 8 + e]) * inv);
+                    *reinterpret_cast<uint4 *>(dst + c8 * 8) = *reinterpret_cast<const uint4 *>(v);
                 }
             }
         }
@@ -614,8 +799,7 @@ bool prefill_supported(int dtype, int head_dim, int block_size) {
 }
 
 cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k_cache,
-                           const void *v_cache, int dtype, int max_query_len,
-                           cudaStream_t stream) {
+                           const void *v_cache, int dtype, int num_sms, cudaStream_t stream) {
     const bool bf16 = dtype == PA_DTYPE_BF16;
     const int H = args.num_heads;
     CUtensorMap tm_q, tm_k, tm_v;
@@ -654,10 +838,9 @@ cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    const int pairs = (max_query_len + kTiles * kBM - 1) / (kTiles * kBM);
-    if (pairs > 65535) return cudaErrorInvalidValue;
-    cfg.gridDim = dim3(static_cast<unsigned>(H), static_cast<unsigned>(args.num_seqs),
-                       static_cast<unsigned>(pairs));
+    // persistent: one CTA per SM (the shared memory allows no second one)
+    const long long items = static_cast<long long>(args.num_pairs) * args.num_seqs * H;
+    cfg.gridDim = dim3(static_cast<unsigned>(items < num_sms ? items : num_sms));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

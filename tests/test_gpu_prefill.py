@@ -104,3 +104,42 @@ def test_prefill_rising_maximum(dev, dtype):
     ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
                          case.context_lens, case.query_start, case.scale, dtype=dtype)
     assert_parity(got, ref, f"prefill rising {dtype}", dtype=dtype)
+
+
+def test_prefill_counters_reused_and_left_zero(dev):
+    """One work-queue counter buffer across calls of different shapes: each
+    result matches the oracle and the kernel leaves the counters at zero."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    ctr = torch.zeros(2, dtype=torch.int32, device=dev)
+    shapes = [([700, 33, 256], [700, 20, 256]), ([1, 2, 3], [1, 2, 3]), ([513, 1000], [300, 1000])]
+    for i, (ctx, ql) in enumerate(shapes):
+        case = workloads.build_prefill_case(f"pf_ctr{i}", np.array(ctx), np.array(ql), num_heads=3,
+                                            head_dim=128, seed=60 + i)
+        d = upload(case, dev)
+        qs = torch.from_numpy(case.query_start).to(dev)
+        out = torch.full(case.q.shape, float("nan"), dtype=torch.float16, device=dev)
+        pa.prefill(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                   qs, case.scale, counters=ctr)
+        torch.cuda.synchronize(dev)
+        assert pa.device_errors() == 0
+        assert ctr.cpu().tolist() == [0, 0]
+        ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
+                             case.context_lens, case.query_start, case.scale)
+        assert_parity(to_numpy(out, case), ref, f"prefill counters call {i}")
+
+
+def test_prefill_library_allocated_counters(dev):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    case = workloads.build_prefill_case("pf_lib", np.array([300, 129]), np.array([300, 64]),
+                                        num_heads=2, head_dim=128, seed=70)
+    d = upload(case, dev)
+    qs = torch.from_numpy(case.query_start).to(dev)
+    out = torch.full(case.q.shape, float("nan"), dtype=torch.float16, device=dev)
+    pa.prefill(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], qs,
+               case.scale, allocate_in_library=True)
+    assert pa.device_errors() == 0
+    ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+                         case.query_start, case.scale)
+    assert_parity(to_numpy(out, case), ref, "prefill, library-allocated counters")

@@ -77,6 +77,12 @@ constexpr int kRegsSoftmax = PA_PREFILL_REGS_SOFTMAX;
 constexpr int kRegsOther = PA_PREFILL_REGS_OTHER;
 static_assert(2 * kRegsSoftmax + kRegsOther <= 3 * 168, "register split exceeds the launch");
 static_assert(kRegsSoftmax % 8 == 0 && kRegsOther % 8 == 0 && kRegsOther >= 24, "bad split");
+// 1: the two MMA threads take turns, batch (0, j) -> (1, j) -> (0, j + 1),
+// so one tile's softmax overlaps the other tile's products; 0: they issue
+// independently.
+#ifndef PA_PREFILL_PINGPONG
+#define PA_PREFILL_PINGPONG 1
+#endif
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;      // S_t / P_t: columns 128 t .. 128 t + 127
@@ -106,7 +112,8 @@ enum Bar {
     O_EMPTY = 19,        // [tile], the epilogue has read O_t
     ITEM_FULL = 21,      // [slot] of the work-item ring
     ITEM_EMPTY = 23,     // [slot]
-    kNumBars = 25
+    TURN = 25,           // [tile]: the MMA thread of tile t has issued a batch
+    kNumBars = 27
 };
 // K_EMPTY, V_EMPTY and Q_EMPTY take one arrival from each MMA thread; a
 // thread arrives on an EMPTY barrier only after waiting for the matching
@@ -532,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t g = 0;      // key tiles consumed, over all items
             uint32_t pc = 0;     // P_FULL phases consumed
             uint32_t oc = 0;     // items in which this query tile was active
+            uint32_t turns = 0;  // TURN phases of the other thread consumed
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int slot = k % 2;
@@ -544,6 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 item_geometry(a, w, false, it);
                 const bool active = t < it.ntiles;
                 const int nk = active ? tile_key_tiles(it, t) : 0;
+                // key tiles of the other query tile (0 when it is idle)
+                const int nk_other = (1 - t) < it.ntiles ? tile_key_tiles(it, 1 - t) : 0;
                 ok = mbar_wait(&bar[Q_FULL], k & 1, abort_flag, a.err) &&
                      mbar_wait(&bar[K_FULL + g % kStages], (g / kStages) & 1, abort_flag, a.err);
                 if (!ok) break;
@@ -570,6 +580,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // epilogue has read it
                         if (ok && j == 0 && oc > 0)
                             ok = mbar_wait(&bar[O_EMPTY + t], (oc - 1) & 1, abort_flag, a.err);
+#if PA_PREFILL_PINGPONG
+                        // batch (1, j) follows (0, j); batch (0, j) follows (1, j - 1)
+                        const bool wait_turn = t == 1 ? j < nk_other : (j >= 1 && j - 1 < nk_other);
+                        if (ok && wait_turn) {
+                            ok = mbar_wait(&bar[TURN + 1 - t], turns & 1, abort_flag, a.err);
+                            ++turns;
+                        }
+#endif
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
@@ -580,6 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        smem_desc(v_addr + st * kTileBytes + ks * 2048, kHalf, 1024),
                                        idesc_pv, j > 0 || pass > 0 || ks > 0);
                         mma_commit(&bar[V_EMPTY + st]);
+#if PA_PREFILL_PINGPONG
+                        // the other thread's next batch waits for this one
+                        const bool give_turn = t == 0 ? j < nk_other : j + 1 < nk_other;
+#endif
                         if (j + 1 < nk) {
                             ok = mbar_wait(&bar[K_FULL + st1], ((g + 1) / kStages) & 1, abort_flag,
                                            a.err);
@@ -589,9 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_commit(&bar[S_FULL + t]);
                             mma_commit(&bar[K_EMPTY + st1]);
                             if (j + 2 == nk) mma_commit(&bar[Q_EMPTY]);  // last S issued
+#if PA_PREFILL_PINGPONG
+                            if (give_turn) mbar_arrive(&bar[TURN + t]);
+#endif
                             continue;
                         }
                         mma_commit(&bar[O_FULL + t]);
+#if PA_PREFILL_PINGPONG
+                        if (give_turn) mbar_arrive(&bar[TURN + t]);
+#endif
                     } else {
                         mbar_arrive(&bar[V_EMPTY + st]);
                     }

@@ -89,6 +89,32 @@ def decode_source_hash():
     return h.hexdigest()[:16]
 
 
+PREFILL_SOURCES = ("paged_kv_cache_269_gb300/csrc/pa_prefill.cu",)
+
+
+def recorded_prefill_traffic(workload):
+    """DRAM bytes (read + write) per prefill launch from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"pa_prefill_{workload.replace('prefill_', '')}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path, encoding="utf-8"):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for rel in PREFILL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if vals.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+        return None
+    try:
+        return int(float(vals["dram_bytes_read"]) + float(vals["dram_bytes_write"]))
+    except (KeyError, ValueError):
+        return None
+
+
 def recorded_traffic(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
@@ -581,6 +607,7 @@ def run_prefill_op(args, local_rank):
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "peak_source": src,
                      "algorithmic_flops_per_launch": int(flops),
+                     "traffic": recorded_prefill_traffic(wl), "traffic_unit": "DRAM bytes per launch",
                      "note": "algorithmic flops: 4*D per causal (query, key) pair per head; "
                              "the kernel issues 1.5x (P V runs for P_hi and P_lo)"},
         "gpu_launches": args.steps}))

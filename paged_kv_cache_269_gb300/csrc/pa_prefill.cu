@@ -30,11 +30,10 @@
 //    running maximum that is only raised when a tile's maximum exceeds it
 //    by more than 8 (so weights stay below 2^14, inside fp16's range);
 //    raising it rescales O_t in tensor memory.  The weights go back into the
-//    same tensor-memory columns as a 16-bit pair P_hi + P_lo (P_hi is the
-//    weight truncated to the format's precision, P_lo the rounded
-//    remainder), which carries about 21 bits, so small outputs meet the
-//    same relative bound as decode.  The row sum stays in fp32; the
-//    epilogue divides O_t by it.
+//    same tensor-memory columns as a 16-bit pair P_hi + P_lo (P_hi the
+//    weight rounded to the format, P_lo the rounded remainder), which
+//    carries about 22 bits, so small outputs meet the same relative bound as
+//    decode.  The row sum stays in fp32; the epilogue divides O_t by it.
 //  * Tensor-memory columns: S_0/P_0 0-127, S_1/P_1 128-255, O_0 256-383,
 //    O_1 384-511 (the whole of the SM's tensor memory: one CTA per SM).
 //  * Every wait is bounded; tensor memory is released on every path.
@@ -273,17 +272,30 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, in
 }
 
 // The weight pair (P_hi, P_lo) of two consecutive keys, packed as the MMA
-// reads A from tensor memory.  P_hi = the weight with its fp32 mantissa cut to
-// the 16-bit format's width (exact in that format for weights in its normal
-// range), P_lo = the remainder rounded to nearest.
+// reads A from tensor memory (lower key in the low half).  P_hi = the weight
+// rounded to the 16-bit format, P_lo = the remainder p - P_hi (exact in
+// fp32) rounded to the format.  PA_PREFILL_SPLIT_RN=0 takes P_hi by cutting
+// the fp32 mantissa instead (one more integer op per weight).
+#ifndef PA_PREFILL_SPLIT_RN
+#define PA_PREFILL_SPLIT_RN 1
+#endif
 struct F16T {
     static constexpr bool kBf16 = false;
     __device__ static __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+#if PA_PREFILL_SPLIT_RN
+        // P_hi = p rounded to fp16, widened back exactly; P_lo = the rounded
+        // remainder
+        const __half2 h = __floats2half2_rn(p0, p1);
+        const float2 hf = __half22float2(h);
+        float l0, l1;
+        sub2(l0, l1, p0, p1, hf.x, hf.y);
+#else
         const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
         const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
         float l0, l1;
         sub2(l0, l1, p0, p1, h0, h1);
         const __half2 h = __floats2half2_rn(h0, h1);
+#endif
         const __half2 l = __floats2half2_rn(l0, l1);
         hi = *reinterpret_cast<const uint32_t *>(&h);
         lo = *reinterpret_cast<const uint32_t *>(&l);
@@ -296,10 +308,17 @@ struct F16T {
 struct BF16T {
     static constexpr bool kBf16 = true;
     __device__ static __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+#if PA_PREFILL_SPLIT_RN
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        hi = *reinterpret_cast<const uint32_t *>(&h);
+        float l0, l1;
+        sub2(l0, l1, p0, p1, __uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+#else
         const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
         hi = __byte_perm(b0, b1, 0x7632);   // upper halves: the truncated bf16 values
         float l0, l1;
         sub2(l0, l1, p0, p1, __uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u));
+#endif
         const __nv_bfloat162 l = __floats2bfloat162_rn(l0, l1);
         lo = *reinterpret_cast<const uint32_t *>(&l);
     }

@@ -9,33 +9,38 @@
 //
 // How: this is the one dense contraction of the paged cache, so it runs on
 // the 5th-generation tensor cores with every accumulator in tensor memory.
-//  * One CTA per (pair of 128-query tiles, head, sequence); ten warps.  The
-//    two query tiles share every K/V tile and take turns on the tensor core:
-//    while one tile's softmax runs, the other tile's MMAs do.
-//  * Warp 8 (TMA): loads both Q tiles once and, per tile of 128 keys, the
-//    eight 16-token K and V blocks named by the block table as 2-D
-//    tensor-map boxes (64 dims x 16 tokens) that land directly in the
-//    128-byte-swizzled operand layouts; two stages each for K and V.  Rows
-//    of the last V tile past the last key are zeroed before use (a zero
-//    weight times a NaN from an unused slot would still be NaN).
-//  * Warp 9 (MMA): S_t = Q_t K^T (M 128, N 128, K 128) into tensor memory;
-//    once softmax t has published P_t, O_t += P_hi V + P_lo V (M 128, N 128,
-//    K 128; P read from tensor memory, V as an MN-major operand), then
-//    S_t of the next key tile.  Order per key tile j:
-//    PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
-//  * Warps 0-3 / 4-7 (softmax of tile 0 / 1): thread = query row (the
-//    tensor-memory lane of an M = 128 accumulator).  It reads its 128
-//    scores, masks the causal boundary, and turns them into weights
-//    2^(x - m + 6) in fp32, where x is the score in the log2 domain and m a
-//    running maximum that is only raised when a tile's maximum exceeds it
-//    by more than 8 (so weights stay below 2^14, inside fp16's range);
-//    raising it rescales O_t in tensor memory.  The weights go back into the
-//    same tensor-memory columns as a 16-bit pair P_hi + P_lo (P_hi the
-//    weight rounded to the format, P_lo the rounded remainder), which
-//    carries about 22 bits, so small outputs meet the same relative bound as
-//    decode.  The row sum stays in fp32; the epilogue divides O_t by it.
-//  * Tensor-memory columns: S_0/P_0 0-127, S_1/P_1 128-255, O_0 256-383,
-//    O_1 384-511 (the whole of the SM's tensor memory: one CTA per SM).
+//  * Persistent: one CTA per SM takes work items -- (pair of 128-query
+//    tiles, sequence, head), heaviest first -- from an atomic counter.
+//  * Warp 8 (TMA): publishes each item to the other roles through a
+//    two-slot ring, loads its two Q tiles once and, per tile of 64 keys, the
+//    four 16-token K and V blocks named by the block table as 2-D tensor-map
+//    boxes (64 dims x 16 tokens) that land directly in the 128-byte-swizzled
+//    operand layouts; three stages each for K and V.  Rows of an item's last
+//    V tile past its last key are zeroed before use (a zero weight times a
+//    NaN from an unused slot would still be NaN).
+//  * Warps 9-12 issue the tensor-core products, one thread each, so four
+//    instruction streams keep the tensor core busy (one thread's stream
+//    alone is limited by the issue latency of each tcgen05.mma):
+//      warps 9, 10: S_t = Q_t K^T (M 128, N 64, K 128) for query tile t, into
+//        one of two tensor-memory S/P buffers, ahead of the softmax, once the
+//        P V product that last read the buffer is complete;
+//      warps 11, 12: once softmax t has published P_t, O_t += P_hi V +
+//        P_lo V (M 128, N 128, K 64; P read from tensor memory, V as an
+//        MN-major operand).
+//  * Warps 0-3 / 4-7 (softmax of query tile 0 / 1): thread = query row (the
+//    tensor-memory lane of an M = 128 accumulator).  It reads its 64 scores,
+//    masks the causal boundary, and turns them into weights 2^(x - m + 6) in
+//    fp32, where x is the score in the log2 domain and m a running maximum
+//    that is only raised when a tile's maximum exceeds it by more than 8 (so
+//    weights stay below 2^14, inside fp16's range); raising it rescales O_t
+//    in tensor memory once the previous P V product is done.  The weights go
+//    back into the same tensor-memory columns as a 16-bit pair P_hi + P_lo
+//    (P_hi the weight rounded to the format, P_lo the rounded remainder),
+//    which carries about 22 bits, so small outputs meet the same relative
+//    bound as decode.  The row sum stays in fp32; the epilogue divides O_t
+//    by it.
+//  * Tensor-memory columns: S/P buffers of tile t at 128 t and 128 t + 64,
+//    O_0 at 256, O_1 at 384 (the whole of the SM's tensor memory).
 //  * Every wait is bounded; tensor memory is released on every path.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,68 +60,68 @@ namespace {
 constexpr int kD = 128;             // head_dim
 constexpr int kBM = 128;            // query rows per tile (MMA M)
 constexpr int kTiles = 2;           // query tiles per CTA
-constexpr int kBN = 128;            // keys per tile
+constexpr int kBN = 64;             // keys per tile
 constexpr int kB = 16;              // block_size
 constexpr int kBlocksPerTile = kBN / kB;
-constexpr int kStages = 2;
-constexpr int kThreads = 384;       // 2 x 4 softmax warps; TMA warp, 2 MMA warps, 1 idle warp
+constexpr int kStages = 3;          // K and V ring depth
+constexpr int kSBufs = 2;           // S/P buffers per query tile
+constexpr int kThreads = 512;       // 2 x 4 softmax warps; TMA warp, 4 MMA-issuing warps, 3 idle
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp0 = 9;        // issues query tile 0's products; warp 10 tile 1's
-// Register split: launched at 168 per thread (384 threads), the third
-// warpgroup (TMA, MMA, idle) gives registers up to the two softmax
-// warpgroups; the three shares must fit the block's launch allotment of
-// 3 x 168 per lane.
+constexpr int kSWarp0 = 9;          // issues query tile 0's S products; warp 10 tile 1's
+constexpr int kPvWarp0 = 11;        // issues query tile 0's P V products; warp 12 tile 1's
+// Register split: launched at 128 per thread (512 threads), the two
+// producer warpgroups (warps 8-15) give registers up to the two softmax
+// warpgroups; the four shares must fit the block's launch allotment of
+// 4 x 128 per lane.
 #ifndef PA_PREFILL_REGS_SOFTMAX
 #define PA_PREFILL_REGS_SOFTMAX 208
 #endif
 #ifndef PA_PREFILL_REGS_OTHER
-#define PA_PREFILL_REGS_OTHER 88
+#define PA_PREFILL_REGS_OTHER 48
 #endif
 constexpr int kRegsSoftmax = PA_PREFILL_REGS_SOFTMAX;
 constexpr int kRegsOther = PA_PREFILL_REGS_OTHER;
-static_assert(2 * kRegsSoftmax + kRegsOther <= 3 * 168, "register split exceeds the launch");
+static_assert(2 * kRegsSoftmax + 2 * kRegsOther <= 4 * 128, "register split exceeds the launch");
 static_assert(kRegsSoftmax % 8 == 0 && kRegsOther % 8 == 0 && kRegsOther >= 24, "bad split");
-// 1: the two MMA threads take turns, batch (0, j) -> (1, j) -> (0, j + 1),
-// so one tile's softmax overlaps the other tile's products; 0: they issue
-// independently.
-#ifndef PA_PREFILL_PINGPONG
-#define PA_PREFILL_PINGPONG 1
-#endif
-
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;      // S_t / P_t: columns 128 t .. 128 t + 127
+constexpr uint32_t kTmemS = 0;      // S/P buffer b of tile t: columns 128 t + 64 b .. + 63
 constexpr uint32_t kTmemO = 256;    // O_t: columns 256 + 128 t .. 256 + 128 t + 127
 constexpr float kRescaleLog2 = 8.f; // raise the running maximum only past this margin
 constexpr float kBiasLog2 = 6.f;    // weights are 2^(x - m + 6): at most 2^14
 
 // shared memory layout (bytes; tiles 1024-aligned for the 128B swizzle)
-constexpr int kHalf = 128 * 128;               // one 64-dim half of a 128-row tile
-constexpr int kTileBytes = 2 * kHalf;          // Q tile, K tile or V tile: 32 KiB
+constexpr int kHalfQ = kBM * 128;              // one 64-dim half of a Q tile
+constexpr int kTileQ = 2 * kHalfQ;             // 32 KiB
+constexpr int kHalfKV = kBN * 128;             // one 64-dim half of a K or V tile
+constexpr int kTileKV = 2 * kHalfKV;           // 16 KiB
 constexpr int OFF_Q = 0;                       // [tile][half][128 rows][128 B]
-constexpr int OFF_K = OFF_Q + kTiles * kTileBytes;   // [stage][half][128 keys][128 B]
-constexpr int OFF_V = OFF_K + kStages * kTileBytes;
-constexpr int OFF_BAR = OFF_V + kStages * kTileBytes;
+constexpr int OFF_K = OFF_Q + kTiles * kTileQ; // [stage][half][64 keys][128 B]
+constexpr int OFF_V = OFF_K + kStages * kTileKV;
+constexpr int OFF_BAR = OFF_V + kStages * kTileKV;
 enum Bar {
     Q_FULL = 0,
-    K_FULL = 1,          // [stage]
-    K_EMPTY = 3,         // [stage]
-    V_FULL = 5,          // [stage]
-    V_EMPTY = 7,         // [stage]
-    V_ZERO = 9,          // an item's last V tile loaded and its tail rows cleared
-    S_FULL = 10,         // [tile]
-    P_FULL = 12,         // [tile], one arrival per softmax warp
-    O_FULL = 14,         // [tile]
-    MMA_DONE = 16,       // [tile]
-    Q_EMPTY = 18,        // every S product of the item complete (one arrival per MMA thread)
-    O_EMPTY = 19,        // [tile], the epilogue has read O_t
-    ITEM_FULL = 21,      // [slot] of the work-item ring
-    ITEM_EMPTY = 23,     // [slot]
-    TURN = 25,           // [tile]: the MMA thread of tile t has issued a batch
-    kNumBars = 27
+    Q_EMPTY = 1,         // every S product of the item complete, one arrival per S thread
+    K_FULL = 2,          // [stage]
+    K_EMPTY = 5,         // [stage], one arrival per S thread
+    V_FULL = 8,          // [stage]
+    V_EMPTY = 11,        // [stage], one arrival per P V thread
+    V_ZERO = 14,         // an item's last V tile loaded and its tail rows cleared
+    S_FULL = 15,         // [tile][buffer]
+    P_FULL = 19,         // [tile][buffer], one arrival per softmax warp
+    PV_DONE = 23,        // [tile][buffer]: the P V product reading the buffer is complete
+    O_FULL = 27,         // [tile]
+    O_EMPTY = 29,        // [tile], the epilogue has read O_t (one arrival per softmax warp)
+    MMA_DONE = 31,       // [issuing thread]
+    ITEM_FULL = 35,      // [slot] of the work-item ring
+    ITEM_EMPTY = 37,     // [slot]: the 4 MMA threads and the 8 softmax warps
+    kNumBars = 39
 };
-// K_EMPTY, V_EMPTY and Q_EMPTY take one arrival from each MMA thread; a
-// thread arrives on an EMPTY barrier only after waiting for the matching
-// FULL phase, so an arrival can never count toward an earlier phase.
+// K_EMPTY and Q_EMPTY take one arrival from each S thread, V_EMPTY one from
+// each P V thread; a thread arrives on an
+// EMPTY barrier only after waiting for the matching FULL phase, so an
+// arrival can never count toward an earlier phase.  The per-buffer barriers
+// (S_FULL, P_FULL, PV_DONE) never run more than one phase ahead of their
+// waiters, so a parity wait cannot alias.
 constexpr int OFF_TMEM = OFF_BAR + kNumBars * 8;
 constexpr int OFF_FLAG = OFF_TMEM + 8;
 constexpr int OFF_ITEM = OFF_FLAG + 8;              // int[2]
@@ -363,8 +368,9 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
     return true;
 }
 
-// key tiles needed by query tile t of an item
+// key tiles needed by query tile t of an item (0 if the tile is idle)
 __device__ __forceinline__ int tile_key_tiles(const Item &it, int t) {
+    if (t >= it.ntiles) return 0;
     const int rows_t = min(kBM, it.q_len - it.row0 - t * kBM);
     return (it.ctx - it.q_len + it.row0 + t * kBM + rows_t + kBN - 1) / kBN;
 }
@@ -387,13 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == P_FULL || i == P_FULL + 1 || i == O_EMPTY || i == O_EMPTY + 1)
+            if ((i >= P_FULL && i < P_FULL + 4) || i == O_EMPTY || i == O_EMPTY + 1)
                 count = 4;                       // one arrival per softmax warp
             else if (i == ITEM_EMPTY || i == ITEM_EMPTY + 1)
-                count = 10;                      // the 2 MMA threads and the 8 softmax warps
-            else if (i == K_EMPTY || i == K_EMPTY + 1 || i == V_EMPTY || i == V_EMPTY + 1 ||
-                     i == Q_EMPTY)
-                count = 2;                       // the 2 MMA threads
+                count = 12;                      // the 4 MMA threads and the 8 softmax warps
+            else if ((i >= K_EMPTY && i < K_EMPTY + kStages) ||
+                     (i >= V_EMPTY && i < V_EMPTY + kStages) || i == Q_EMPTY)
+                count = 2;                       // the 2 S threads / the 2 P V threads
             mbar_init(&bar[i], count);
         }
         *abort_flag = 0;
@@ -450,10 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar[Q_FULL], it.ntiles * kTileBytes);
+                mbar_arrive_expect_tx(&bar[Q_FULL], it.ntiles * kTileQ);
                 for (int t = 0; t < it.ntiles; ++t)
                     for (int half = 0; half < 2; ++half)
-                        tma_load_3d(smem + OFF_Q + t * kTileBytes + half * kHalf, &tm_q, half * 64,
+                        tma_load_3d(smem + OFF_Q + t * kTileQ + half * kHalfQ, &tm_q, half * 64,
                                     it.h, it.q_first + it.row0 + t * kBM, &bar[Q_FULL]);
             }
             ++q_loads;
@@ -462,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < it.nkt && ok; ++j) {
                 const int st = gk % kStages;
                 const uint32_t ph = (gk / kStages) & 1;
-                // physical blocks of this key tile: lane i < 8 looks up block i
+                // physical blocks of this key tile: lane i < 4 looks up block i
                 int phys = -1;
                 const int b = j * kBlocksPerTile + lane;
                 if (lane < kBlocksPerTile && b < nblk_needed) {
@@ -480,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&bar[K_FULL + st], bytes);
                 __syncwarp();
                 if (phys >= 0) {
-                    uint8_t *dst = smem + OFF_K + st * kTileBytes + lane * (kB * 128);
+                    uint8_t *dst = smem + OFF_K + st * kTileKV + lane * (kB * 128);
                     tma_load_2d(dst, &tm_k, 0, y, &bar[K_FULL + st]);
-                    tma_load_2d(dst + kHalf, &tm_k, 64, y, &bar[K_FULL + st]);
+                    tma_load_2d(dst + kHalfKV, &tm_k, 64, y, &bar[K_FULL + st]);
                 }
                 ++gk;
                 ok = warp_all(mbar_wait(&bar[V_EMPTY + st], ph ^ 1, abort_flag, a.err));
@@ -490,9 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&bar[V_FULL + st], bytes);
                 __syncwarp();
                 if (phys >= 0) {
-                    uint8_t *dst = smem + OFF_V + st * kTileBytes + lane * (kB * 128);
+                    uint8_t *dst = smem + OFF_V + st * kTileKV + lane * (kB * 128);
                     tma_load_2d(dst, &tm_v, 0, y, &bar[V_FULL + st]);
-                    tma_load_2d(dst + kHalf, &tm_v, 64, y, &bar[V_FULL + st]);
+                    tma_load_2d(dst + kHalfKV, &tm_v, 64, y, &bar[V_FULL + st]);
                 }
                 ++gv;
                 if (j == it.nkt - 1) {
@@ -500,10 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = warp_all(mbar_wait(&bar[V_FULL + st], ph, abort_flag, a.err));
                     if (!ok) break;
                     const int first_zero = it.kmax - j * kBN;
-                    uint8_t *vt = smem + OFF_V + st * kTileBytes;
+                    uint8_t *vt = smem + OFF_V + st * kTileKV;
                     for (int idx = lane; idx < (kBN - first_zero) * 16; idx += 32) {
                         const int key = first_zero + idx / 16, half = (idx / 8) % 2, c = idx % 8;
-                        *reinterpret_cast<uint4 *>(vt + half * kHalf + key * 128 + c * 16) =
+                        *reinterpret_cast<uint4 *>(vt + half * kHalfKV + key * 128 + c * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -531,34 +537,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-      } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
-        // ------------------------------------------------------------ MMA
-        // One thread per query tile, so the two tiles' issue streams (and
-        // their waits) proceed independently; each thread's own products
-        // execute in issue order, which keeps S_t(j + 1) behind the P_t V
-        // product that reads the same tensor-memory columns.
+      } else if (warp == kSWarp0 || warp == kSWarp0 + 1) {
+        // ------------------------------------------------------------ S
+        // One thread per query tile t: S_t(n) = Q_t K^T into buffer n % 2,
+        // once the P V product that last read that buffer (number n - 2) is
+        // complete; the buffers let S run two key tiles ahead of the
+        // softmax.  Every K tile of an item receives one EMPTY arrival from
+        // each of the two threads.
         if (lane == 0) {
-            const int t = warp - kMmaWarp0;
+            const int t = warp - kSWarp0;
             constexpr uint32_t idesc_s = instr_desc(E::kBf16, false, kBN);
-            constexpr uint32_t idesc_pv = instr_desc(E::kBf16, true, kD);
-            const uint32_t q_addr = smem_addr(smem + OFF_Q) + t * kTileBytes;
+            const uint32_t q_addr = smem_addr(smem + OFF_Q) + t * kTileQ;
             const uint32_t k_addr = smem_addr(smem + OFF_K);
-            const uint32_t v_addr = smem_addr(smem + OFF_V);
-            const uint32_t tm_s = tmem + kTmemS + t * 128;
-            const uint32_t tm_o = tmem + kTmemO + t * 128;
-            auto issue_s = [&](int st) {
-#pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {  // S_t = Q_t K^T over the 128 dims
-                    const int half = ks / 4, kk = ks % 4;
-                    mma_ss(tm_s, smem_desc(q_addr + half * kHalf + kk * 32, 16, 1024),
-                           smem_desc(k_addr + st * kTileBytes + half * kHalf + kk * 32, 16, 1024),
-                           idesc_s, ks > 0);
-                }
-            };
-            uint32_t g = 0;      // key tiles consumed, over all items
-            uint32_t pc = 0;     // P_FULL phases consumed
-            uint32_t oc = 0;     // items in which this query tile was active
-            uint32_t turns = 0;  // TURN phases of the other thread consumed
+            uint32_t g = 0;      // K tiles consumed, over all items
+            uint32_t ns = 0;     // S products issued
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int slot = k % 2;
@@ -569,91 +561,103 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (w < 0) break;
                 Item it;
                 item_geometry(a, w, false, it);
-                const bool active = t < it.ntiles;
-                const int nk = active ? tile_key_tiles(it, t) : 0;
-                // key tiles of the other query tile (0 when it is idle)
-                const int nk_other = (1 - t) < it.ntiles ? tile_key_tiles(it, 1 - t) : 0;
-                ok = mbar_wait(&bar[Q_FULL], k & 1, abort_flag, a.err) &&
-                     mbar_wait(&bar[K_FULL + g % kStages], (g / kStages) & 1, abort_flag, a.err);
-                if (!ok) break;
-                if (active) {
-                    tc_fence_after();
-                    issue_s(g % kStages);
-                    mma_commit(&bar[S_FULL + t]);
-                    mma_commit(&bar[K_EMPTY + g % kStages]);
-                    if (nk == 1) mma_commit(&bar[Q_EMPTY]);
-                } else {
-                    mbar_arrive(&bar[K_EMPTY + g % kStages]);
-                    mbar_arrive(&bar[Q_EMPTY]);
-                }
+                const int nk = tile_key_tiles(it, t);
+                ok = mbar_wait(&bar[Q_FULL], k & 1, abort_flag, a.err);
+                if (ok && nk == 0) mbar_arrive(&bar[Q_EMPTY]);   // this query tile is idle
                 for (int j = 0; j < it.nkt && ok; ++j, ++g) {
-                    const int st = g % kStages, st1 = (g + 1) % kStages;
+                    const int st = g % kStages;
+                    ok = mbar_wait(&bar[K_FULL + st], (g / kStages) & 1, abort_flag, a.err);
+                    if (!ok) break;
+                    if (j >= nk) {
+                        mbar_arrive(&bar[K_EMPTY + st]);
+                        continue;
+                    }
+                    const uint32_t buf = ns % kSBufs;
+                    if (ns >= kSBufs)   // the buffer's previous reader
+                        ok = mbar_wait(&bar[PV_DONE + t * kSBufs + buf], ((ns - kSBufs) / kSBufs) & 1,
+                                       abort_flag, a.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t tm_s = tmem + kTmemS + t * 128 + buf * 64;
+#pragma unroll
+                    for (int ks = 0; ks < kD / 16; ++ks) {  // over the 128 dims
+                        const int half = ks / 4, kk = ks % 4;
+                        mma_ss(tm_s, smem_desc(q_addr + half * kHalfQ + kk * 32, 16, 1024),
+                               smem_desc(k_addr + st * kTileKV + half * kHalfKV + kk * 32, 16, 1024),
+                               idesc_s, ks > 0);
+                    }
+                    mma_commit(&bar[S_FULL + t * kSBufs + buf]);
+                    ++ns;
+                    mma_commit(&bar[K_EMPTY + st]);
+                    if (j == nk - 1) mma_commit(&bar[Q_EMPTY]);   // this tile's last S
+                }
+            }
+            // make sure none of this thread's products is still running when
+            // the CTA releases TMEM
+            mma_commit(&bar[MMA_DONE + t]);
+            mbar_wait_drain(&bar[MMA_DONE + t], 0);
+        }
+        __syncwarp();
+      } else if (warp == kPvWarp0 || warp == kPvWarp0 + 1) {
+        // ------------------------------------------------------------ P V
+        // One thread per query tile t: O_t += P_hi V + P_lo V for each key
+        // tile, once softmax t has published P_t.  Every V tile of an item
+        // receives one EMPTY arrival from each of the two threads.
+        if (lane == 0) {
+            const int t = warp - kPvWarp0;
+            constexpr uint32_t idesc_pv = instr_desc(E::kBf16, true, kD);
+            const uint32_t v_addr = smem_addr(smem + OFF_V);
+            const uint32_t tm_s = tmem + kTmemS + t * 128;   // + 64 b for buffer b
+            const uint32_t tm_o = tmem + kTmemO + t * 128;
+            uint32_t g = 0;      // V tiles consumed, over all items
+            uint32_t np = 0;     // P_t tiles consumed (buffer = np % 2)
+            uint32_t oc = 0;     // items in which this query tile was active
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int slot = k % 2;
+                ok = mbar_wait(&bar[ITEM_FULL + slot], (k / 2) & 1, abort_flag, a.err);
+                if (!ok) break;
+                const int w = item_ring[slot];
+                mbar_arrive(&bar[ITEM_EMPTY + slot]);
+                if (w < 0) break;
+                Item it;
+                item_geometry(a, w, false, it);
+                const int nk = tile_key_tiles(it, t);
+                for (int j = 0; j < it.nkt && ok; ++j, ++g) {
+                    const int st = g % kStages;
                     const bool last = j == it.nkt - 1;
                     ok = last ? mbar_wait(&bar[V_ZERO], k & 1, abort_flag, a.err)
                               : mbar_wait(&bar[V_FULL + st], (g / kStages) & 1, abort_flag, a.err);
                     if (!ok) break;
                     if (j < nk) {
-                        ok = mbar_wait(&bar[P_FULL + t], pc & 1, abort_flag, a.err);
-                        ++pc;
+                        const uint32_t buf = np % kSBufs;
+                        ok = mbar_wait(&bar[P_FULL + t * kSBufs + buf], (np / kSBufs) & 1, abort_flag,
+                                       a.err);
                         // O_t still holds the previous item's result until its
                         // epilogue has read it
                         if (ok && j == 0 && oc > 0)
                             ok = mbar_wait(&bar[O_EMPTY + t], (oc - 1) & 1, abort_flag, a.err);
-#if PA_PREFILL_PINGPONG
-                        // batch (1, j) follows (0, j); batch (0, j) follows (1, j - 1)
-                        const bool wait_turn = t == 1 ? j < nk_other : (j >= 1 && j - 1 < nk_other);
-                        if (ok && wait_turn) {
-                            ok = mbar_wait(&bar[TURN + 1 - t], turns & 1, abort_flag, a.err);
-                            ++turns;
-                        }
-#endif
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
                         for (int pass = 0; pass < 2; ++pass)  // O_t += P_hi V + P_lo V
 #pragma unroll
                             for (int ks = 0; ks < kBN / 16; ++ks)
-                                mma_ts(tm_o, tm_s + pass * 64 + ks * 8,
-                                       smem_desc(v_addr + st * kTileBytes + ks * 2048, kHalf, 1024),
+                                mma_ts(tm_o, tm_s + buf * 64 + pass * 32 + ks * 8,
+                                       smem_desc(v_addr + st * kTileKV + ks * 2048, kHalfKV, 1024),
                                        idesc_pv, j > 0 || pass > 0 || ks > 0);
+                        mma_commit(&bar[PV_DONE + t * kSBufs + buf]);
                         mma_commit(&bar[V_EMPTY + st]);
-#if PA_PREFILL_PINGPONG
-                        // the other thread's next batch waits for this one
-                        const bool give_turn = t == 0 ? j < nk_other : j + 1 < nk_other;
-#endif
-                        if (j + 1 < nk) {
-                            ok = mbar_wait(&bar[K_FULL + st1], ((g + 1) / kStages) & 1, abort_flag,
-                                           a.err);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_s(st1);
-                            mma_commit(&bar[S_FULL + t]);
-                            mma_commit(&bar[K_EMPTY + st1]);
-                            if (j + 2 == nk) mma_commit(&bar[Q_EMPTY]);  // last S issued
-#if PA_PREFILL_PINGPONG
-                            if (give_turn) mbar_arrive(&bar[TURN + t]);
-#endif
-                            continue;
-                        }
-                        mma_commit(&bar[O_FULL + t]);
-#if PA_PREFILL_PINGPONG
-                        if (give_turn) mbar_arrive(&bar[TURN + t]);
-#endif
+                        ++np;
+                        if (j == nk - 1) mma_commit(&bar[O_FULL + t]);
                     } else {
                         mbar_arrive(&bar[V_EMPTY + st]);
                     }
-                    if (!last) {  // the next K tile is not used by this query tile
-                        ok = mbar_wait(&bar[K_FULL + st1], ((g + 1) / kStages) & 1, abort_flag, a.err);
-                        if (!ok) break;
-                        mbar_arrive(&bar[K_EMPTY + st1]);
-                    }
                 }
-                if (active) ++oc;
+                if (nk > 0) ++oc;
             }
-            // make sure none of this thread's products is still running when
-            // the CTA releases TMEM
-            mma_commit(&bar[MMA_DONE + t]);
-            mbar_wait_drain(&bar[MMA_DONE + t], 0);
+            mma_commit(&bar[MMA_DONE + 2 + t]);
+            mbar_wait_drain(&bar[MMA_DONE + 2 + t], 0);
         }
         __syncwarp();
       }
@@ -663,12 +667,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp / 4;                      // query tile of this warpgroup
         const int r = (warp % 4) * 32 + lane;        // row within the tile = TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-        const uint32_t s_col = lane_base + kTmemS + t * 128;
+        const uint32_t s_col = lane_base + kTmemS + t * 128;   // + 64 b for buffer b
         const uint32_t o_col = lane_base + kTmemO + t * 128;
         const float c = a.scale_log2;
         const bool scale_pos = c > 0.f;
         const float cm = scale_pos ? c : 1.f;   // multiplier left for the exponent
-        uint32_t s_cnt = 0, o_cnt = 0;          // S_FULL / O_FULL phases consumed
+        uint32_t n = 0;                         // S tiles consumed (buffer = n % 2)
+        uint32_t o_cnt = 0;                     // O_FULL phases consumed
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const int slot = k % 2;
@@ -687,18 +692,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos = r < rows_t ? first_pos + r : -1;   // -1: padding row, all masked
             const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
             float m_used = -INFINITY, l = 0.f;
-            for (int j = 0; j < my_nkt && ok; ++j) {
-                ok = warp_all(mbar_wait(&bar[S_FULL + t], s_cnt & 1, abort_flag, a.err));
-                ++s_cnt;
+            for (int j = 0; j < my_nkt && ok; ++j, ++n) {
+                const uint32_t buf = n % kSBufs;
+                ok = warp_all(mbar_wait(&bar[S_FULL + t * kSBufs + buf], (n / kSBufs) & 1, abort_flag,
+                                        a.err));
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t sb = s_col + buf * 64;
                 float x[kBN];
                 {
                     uint32_t u[kBN];
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        tmem_ld32_nowait(s_col + q4 * 32,
-                                         *reinterpret_cast<uint32_t(*)[32]>(&u[q4 * 32]));
+                    for (int q2 = 0; q2 < kBN / 32; ++q2)
+                        tmem_ld32_nowait(sb + q2 * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[q2 * 32]));
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(u[i]);
@@ -710,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) x[i] *= c;
                 }
-                // causal mask (key j*128 + i visible to this row iff <= pos)
+                // causal mask (key j*64 + i visible to this row iff <= pos)
                 if (j * kBN + kBN - 1 > warp_min_pos) {
                     const int lim = pos - j * kBN;
 #pragma unroll
@@ -742,19 +748,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 add2(sum[0], sum[1], sum[0], sum[1], sum[4], sum[5]);
                 l = l * alpha + (sum[0] + sum[1]);
                 m_used = m_new;
-                // P_t into the S_t columns: P_hi at +0..63, P_lo at +64..127
+                // P_t into the buffer: P_hi at +0..31, P_lo at +32..63
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q2 = 0; q2 < kBN / 32; ++q2) {
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        E::split2(x[q4 * 32 + 2 * e], x[q4 * 32 + 2 * e + 1], hi[e], lo[e]);
-                    tmem_st16(s_col + q4 * 16, hi);
-                    tmem_st16(s_col + 64 + q4 * 16, lo);
+                        E::split2(x[q2 * 32 + 2 * e], x[q2 * 32 + 2 * e + 1], hi[e], lo[e]);
+                    tmem_st16(sb + q2 * 16, hi);
+                    tmem_st16(sb + 32 + q2 * 16, lo);
                 }
-                // a raised maximum rescales O_t (its last update, P V of the
-                // previous tile, completed before this tile's S was signalled)
+                // a raised maximum rescales O_t once the previous tile's P V
+                // product (the last update of O_t) is complete
                 if (j > 0 && !warp_all(alpha == 1.f)) {
+                    const uint32_t pb = (n - 1) % kSBufs;
+                    ok = warp_all(mbar_wait(&bar[PV_DONE + t * kSBufs + pb], ((n - 1) / kSBufs) & 1,
+                                            abort_flag, a.err));
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t ov[32];
@@ -769,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[P_FULL + t]);
+                if (lane == 0) mbar_arrive(&bar[P_FULL + t * kSBufs + buf]);
             }
             if (!ok) break;
             // epilogue: read O_t, hand its columns back to the MMA warp, then

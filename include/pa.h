@@ -381,6 +381,20 @@ int pa_kvm_block_tables(const pa_kv_manager *m, const int32_t *seqs, int32_t num
  */
 int pa_device_errors(void *stream, uint32_t *flags);
 
+/*
+ * pa_selftest_wait_timeout -- check, on the current device, the bounded waits
+ * that every kernel of the library relies on (the pages have no counterpart:
+ * this is failure detection for the library itself).  Launches one CTA on
+ * `stream` that waits on an mbarrier phase nothing completes, then on a
+ * shared-memory word nothing sets, then drains; each wait must give up after
+ * its limit (about 1 s each, so the call takes about 3 s) and record
+ * PA_DEVERR_TIMEOUT.  Synchronises the stream.  results (host, int[3]) gets
+ * 1 for each wait that (wrongly) succeeded, 0 for each that gave up.  The
+ * error word is left set for pa_device_errors to read.  Returns PA_OK or
+ * PA_ERR_CUDA.
+ */
+int pa_selftest_wait_timeout(int32_t *results, void *stream);
+
 /* Human-readable name of a pa_status value. */
 const char *pa_status_string(int status);
 

@@ -11,7 +11,8 @@ Functions (names follow the C ABI):
   reshape_and_cache(k, v, k_cache, v_cache, slot_mapping)
   copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs)
   decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, ...)
-  decode_workspace_bytes(...), decode_counters_bytes(...), device_errors(), version()
+  decode_workspace_bytes(...), decode_counters_bytes(...), device_errors(), version(),
+  selftest_wait_timeout()
 """
 from __future__ import annotations
 
@@ -21,6 +22,7 @@ import threading
 from . import build as _build
 
 __all__ = ["PaError", "Dims", "KVManager", "lib", "reshape_and_cache", "copy_blocks", "decode",
+           "selftest_wait_timeout",
            "prefill", "decode_workspace_bytes",
            "decode_counters_bytes", "device_errors", "reset_workspaces", "version", "DEVERR_TABLE", "DEVERR_CONTEXT",
            "DEVERR_SLOT", "DEVERR_TIMEOUT"]
@@ -41,7 +43,7 @@ EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", 
            "pa_status_string", "pa_last_cuda_error", "pa_version",
            "pa_kvm_create", "pa_kvm_destroy", "pa_kvm_num_free_blocks", "pa_kvm_refcount",
            "pa_kvm_add_sequence", "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free",
-           "pa_kvm_context_len", "pa_kvm_slot", "pa_kvm_block_tables")
+           "pa_kvm_context_len", "pa_kvm_slot", "pa_kvm_block_tables", "pa_selftest_wait_timeout")
 _SIZE_ERROR = (1 << 64) - 1
 
 
@@ -72,6 +74,8 @@ def _declare(l):
     l.pa_copy_blocks.argtypes = [vp, vp, i32, vp, vp, i32, vp, i32, dp, vp]
     l.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp]
     l.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, dp, vp]
+    l.pa_selftest_wait_timeout.argtypes = [vp, vp]
+    l.pa_selftest_wait_timeout.restype = ctypes.c_int
     l.pa_prefill_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, i32, dp, vp,
                                 ctypes.c_size_t, vp]
     l.pa_decode_workspace_bytes.argtypes = [dp, i32, i32]
@@ -496,6 +500,21 @@ class KVManager:
                                            tables.ctypes.data, row_len, lens.ctypes.data),
                "pa_kvm_block_tables")
         return tables, lens
+
+
+def selftest_wait_timeout(stream=None, device=None):
+    """Run the bounded-wait self-test (pa_selftest_wait_timeout, about 3 s):
+    returns, per wait (mbarrier, shared word, drain), 1 if it wrongly
+    succeeded and 0 if it gave up.  PA_DEVERR_TIMEOUT is left in the device
+    error word."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    sh, _ = _stream_handle(device, stream)
+    res = (ctypes.c_int32 * 3)()
+    with torch.cuda.device(device):
+        rc = lib().pa_selftest_wait_timeout(res, sh)
+    _check(rc, "pa_selftest_wait_timeout")
+    return [int(v) for v in res]
 
 
 def device_errors(stream=None, device=None) -> int:

@@ -389,6 +389,24 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
     return e == cudaSuccess ? PA_OK : fail_cuda(e);
 }
 
+int pa_selftest_wait_timeout(int32_t *results, void *stream) {
+    if (!results) return PA_ERR_NULL;
+    DeviceState *st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int *dres = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&dres), 3 * sizeof(int), s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = cudaMemsetAsync(dres, 0xff, 3 * sizeof(int), s);
+    if (e == cudaSuccess) e = launch_wait_timeout_selftest(st->err, dres, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(results, dres, 3 * sizeof(int), cudaMemcpyDeviceToHost, s);
+    const cudaError_t ef = cudaFreeAsync(dres, s);
+    if (e == cudaSuccess) e = ef;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
 int pa_device_errors(void *stream, uint32_t *flags) {
     if (!flags) return PA_ERR_NULL;
     DeviceState *st = nullptr;

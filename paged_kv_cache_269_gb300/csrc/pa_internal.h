@@ -72,6 +72,9 @@ bool prefill_supported(int dtype, int head_dim, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k_cache,
                            const void *v_cache, int dtype, int num_sms, cudaStream_t stream);
 
+// One CTA whose bounded waits must all run out (pa_selftest.cu); result[3].
+cudaError_t launch_wait_timeout_selftest(unsigned int *err, int *result, cudaStream_t stream);
+
 // SM count and device error word of the current device (set up on first use).
 int current_device_info(unsigned int **err, int *num_sms);
 

@@ -258,6 +258,23 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of `values` over all ranks (a list of floats; the
+    same list on one rank)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_value(world, bytes_per_step_per_rank, step_ms):
+    """Whole-job GB/s: every rank moves its bytes in each step; the step time
+    is the slowest rank's."""
+    return world * bytes_per_step_per_rank / (step_ms * 1e-3) / 1e9
+
+
 def config_of(case, args):
     return {"workload": args.workload, "num_seqs": case.num_seqs, "num_heads": case.num_heads,
             "head_dim": case.head_dim, "block_size": case.block_size,
@@ -425,20 +442,14 @@ def run_native(args, rank, world, local_rank):
 
         graph_s = timed(graph_step)
         e2e_s = min(eager_s, graph_s)
-        if dist:
-            tt = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
-        e2e = {"value": round(world * step_bytes(case) / e2e_s / 1e9, 3), "unit": UNIT,
+        e2e_s = max_over_ranks([e2e_s], dist, dev)[0]
+        e2e = {"value": round(job_value(world, step_bytes(case), e2e_s * 1e3), 3), "unit": UNIT,
                "ms_per_step": round(e2e_s * 1e3, 4),
                "ms_per_step_eager": round(eager_s * 1e3, 4),
                "ms_per_step_graph": round(graph_s * 1e3, 4),
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
-    if dist:
-        tt = torch.tensor([step_ms, decode_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms, decode_ms = (float(x) for x in tt.tolist())
+    step_ms, decode_ms = max_over_ranks([step_ms, decode_ms], dist, dev)
 
     if rank != 0:
         return
@@ -446,7 +457,7 @@ def run_native(args, rank, world, local_rank):
     dec_bytes = workloads.decode_algorithmic_bytes(case)
     uniq_bytes = workloads.decode_unique_bytes(case)
     achieved = dec_bytes / (decode_ms * 1e-3) / 1e9
-    value = world * step_bytes(case) / (step_ms * 1e-3) / 1e9
+    value = job_value(world, step_bytes(case), step_ms)
     cpu = None
     if not args.no_cpu_baseline:
         sec, runs, cores = oracle_sample(case, args.cpu_seconds)

@@ -106,3 +106,54 @@ def test_reshape_rejects(lib):
     assert lib.pa_reshape_and_cache(fake, odd, fake, fake, fake, 4, ctypes.byref(d), None) == -4
     bad = _dims(D=80)
     assert lib.pa_reshape_and_cache(fake, fake, fake, fake, fake, 4, ctypes.byref(bad), None) == -3
+
+
+def test_prefill_rejects(lib):
+    fake = ctypes.c_void_p(0x100000)           # never dereferenced: checks fail first
+    d = _dims()
+
+    def call(dims=d, out=fake, total=300, maxq=200, scale=0.1, mb=8, ctr=fake, ctr_n=8):
+        return lib.pa_prefill_ws(out, fake, fake, fake, fake, fake, fake, total, maxq, scale, mb,
+                                 ctypes.byref(dims) if dims is not None else None, ctr, ctr_n, None)
+
+    assert call(dims=None) == -1
+    assert call(dims=_dims(D=64)) == -3          # head_dim 128 only
+    assert call(dims=_dims(B=32)) == -3          # block_size 16 only
+    assert call(dims=_dims(D=0)) == -2
+    assert call(total=-1) == -2
+    assert call(maxq=-1) == -2
+    assert call(mb=0) == -2
+    assert call(dims=_dims(S=0)) == 0            # nothing to do
+    assert call(total=0) == 0
+    assert call(maxq=0) == 0
+    assert call(out=None) == -1
+    assert call(ctr=None) == -1
+    assert call(ctr_n=4) == -5                   # the two work-queue counters need 8 bytes
+    assert call(out=ctypes.c_void_p(0x100002)) == -4
+    assert call(ctr=ctypes.c_void_p(0x100002)) == -4
+    assert call(scale=float("inf")) == -2
+    # more work items (pairs of 128-row tiles x sequences x heads) than an int32 counts
+    assert call(dims=_dims(S=65535, H=65535, N=1), maxq=256) == -2
+    # the allocating entry point validates the same way before any allocation
+    assert lib.pa_prefill(fake, fake, fake, fake, fake, fake, fake, 300, 200, 0.1, 8,
+                          ctypes.byref(_dims(D=64)), None) == -3
+    assert lib.pa_prefill(fake, fake, fake, fake, fake, fake, fake, -1, 200, 0.1, 8,
+                          ctypes.byref(d), None) == -2
+
+
+def test_copy_blocks_rejects(lib):
+    fake = ctypes.c_void_p(0x100000)
+    d = _dims()
+
+    def call(dims=d, n=2, src_n=32, dst_n=32, pairs=fake, dst_k=fake):
+        return lib.pa_copy_blocks(fake, fake, src_n, dst_k, fake, dst_n, pairs, n,
+                                  ctypes.byref(dims) if dims is not None else None, None)
+
+    assert call(dims=None) == -1
+    assert call(n=-1) == -2
+    assert call(src_n=0) == -2
+    assert call(dims=_dims(D=80)) == -3
+    assert call(n=0) == 0                        # nothing to copy
+    assert call(pairs=None) == -1
+    assert call(dst_k=ctypes.c_void_p(0x100008)) == -4
+    assert call(pairs=ctypes.c_void_p(0x100002)) == -4

@@ -143,3 +143,23 @@ def test_prefill_library_allocated_counters(dev):
     ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
                          case.query_start, case.scale)
     assert_parity(to_numpy(out, case), ref, "prefill, library-allocated counters")
+
+
+def test_prefill_bad_table_entry_is_reported(dev):
+    """A block-table entry outside the pool is skipped (never read) and
+    flagged; a clean call afterwards is exact."""
+    import paged_kv_cache_269_gb300 as pa
+    case = workloads.build_prefill_case("pf_badtab", [200, 90], [200, 90], num_heads=2,
+                                        head_dim=128, seed=80)
+    tables = case.block_tables.copy()
+    tables[0, 3] = case.num_blocks + 7
+    case.block_tables = tables
+    _, flags = run_prefill(case, dev)
+    assert flags & pa.DEVERR_TABLE
+    ok = workloads.build_prefill_case("pf_ok", [200, 90], [200, 90], num_heads=2, head_dim=128,
+                                      seed=81)
+    got, flags = run_prefill(ok, dev)
+    assert flags == 0
+    ref = oracle.prefill(ok.q, ok.k_cache, ok.v_cache, ok.block_tables, ok.context_lens,
+                         ok.query_start, ok.scale)
+    assert_parity(got, ref, "prefill after a reported error")

@@ -700,7 +700,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t sb = s_col + buf * 64;
                 float x[kBN];
-                {
+                // the tile's scores, in the log2 domain for a non-positive
+                // scale (for a positive one the scale is folded into the
+                // exponent's FMA), causally masked (key j*64 + i is visible to
+                // this row iff i <= pos - j*64)
+                auto load_scores = [&]() {
                     uint32_t u[kBN];
 #pragma unroll
                     for (int q2 = 0; q2 < kBN / 32; ++q2)
@@ -708,45 +712,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < kBN; ++i) x[i] = __uint_as_float(u[i]);
-                }
-                // scores into the log2 domain: for a positive scale the max of
-                // the raw scores is scaled once and the scale is folded into
-                // the exponent's FMA; otherwise every score is scaled first
-                if (!scale_pos) {
+                    if (!scale_pos) {
 #pragma unroll
-                    for (int i = 0; i < kBN; ++i) x[i] *= c;
-                }
-                // causal mask (key j*64 + i visible to this row iff <= pos)
-                if (j * kBN + kBN - 1 > warp_min_pos) {
-                    const int lim = pos - j * kBN;
-#pragma unroll
-                    for (int i = 0; i < kBN; ++i) x[i] = i <= lim ? x[i] : -INFINITY;
-                }
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int i = 0; i < kBN; i += 8)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) mx[q] = max3(mx[q], x[i + 2 * q], x[i + 2 * q + 1]);
-                const float m_tile = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * cm;
-                float m_new = m_used;
-                if (m_tile > m_used + kRescaleLog2) m_new = m_tile;
-                const float alpha = m_new == m_used ? 1.f : fast_exp2(m_used - m_new);
-                const float bias = m_new == -INFINITY ? 0.f : kBiasLog2 - m_new;
-                float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int i = 0; i < kBN; i += 8) {
-#pragma unroll
-                    for (int q = 0; q < 8; q += 2) {
-                        fma2(x[i + q], x[i + q + 1], x[i + q], x[i + q + 1], cm, cm, bias, bias);
-                        x[i + q] = fast_exp2(x[i + q]);
-                        x[i + q + 1] = fast_exp2(x[i + q + 1]);
-                        add2(sum[q], sum[q + 1], sum[q], sum[q + 1], x[i + q], x[i + q + 1]);
+                        for (int i = 0; i < kBN; ++i) x[i] *= c;
                     }
+                    if (j * kBN + kBN - 1 > warp_min_pos) {
+                        const int lim = pos - j * kBN;
+#pragma unroll
+                        for (int i = 0; i < kBN; ++i) x[i] = i <= lim ? x[i] : -INFINITY;
+                    }
+                };
+                // x <- 2^(x cm + bias) in place; returns the row sum
+                auto exponentiate = [&](float bias) {
+                    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int i = 0; i < kBN; i += 8) {
+#pragma unroll
+                        for (int q = 0; q < 8; q += 2) {
+                            fma2(x[i + q], x[i + q + 1], x[i + q], x[i + q + 1], cm, cm, bias, bias);
+                            x[i + q] = fast_exp2(x[i + q]);
+                            x[i + q + 1] = fast_exp2(x[i + q + 1]);
+                            add2(sum[q], sum[q + 1], sum[q], sum[q + 1], x[i + q], x[i + q + 1]);
+                        }
+                    }
+                    add2(sum[0], sum[1], sum[0], sum[1], sum[2], sum[3]);
+                    add2(sum[4], sum[5], sum[4], sum[5], sum[6], sum[7]);
+                    add2(sum[0], sum[1], sum[0], sum[1], sum[4], sum[5]);
+                    return sum[0] + sum[1];
+                };
+                load_scores();
+                // Optimistic pass: weights against the running maximum.  A row
+                // sum of at most 2^14 proves that no weight exceeds 2^14, i.e.
+                // that the tile's maximum does not exceed the running one by
+                // more than the margin, so the maximum stays and no max pass is
+                // needed.  Otherwise (always on a query tile's first key tile)
+                // the scores are read again -- P has not overwritten them yet
+                // -- and the maximum is taken first.
+                float m_new = m_used, alpha = 1.f, tile_sum = 0.f;
+                bool exact = !warp_all(m_used != -INFINITY);
+                if (!exact) {
+                    tile_sum = exponentiate(kBiasLog2 - m_used);
+                    exact = !warp_all(tile_sum <= 16384.f);
+                    if (exact) load_scores();
                 }
-                add2(sum[0], sum[1], sum[0], sum[1], sum[2], sum[3]);
-                add2(sum[4], sum[5], sum[4], sum[5], sum[6], sum[7]);
-                add2(sum[0], sum[1], sum[0], sum[1], sum[4], sum[5]);
-                l = l * alpha + (sum[0] + sum[1]);
+                if (exact) {
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int i = 0; i < kBN; i += 8)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) mx[q] = max3(mx[q], x[i + 2 * q], x[i + 2 * q + 1]);
+                    const float m_tile = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * cm;
+                    if (m_tile > m_used + kRescaleLog2) m_new = m_tile;
+                    alpha = m_new == m_used ? 1.f : fast_exp2(m_used - m_new);
+                    tile_sum = exponentiate(m_new == -INFINITY ? 0.f : kBiasLog2 - m_new);
+                }
+                l = l * alpha + tile_sum;
                 m_used = m_new;
                 // P_t into the buffer: P_hi at +0..31, P_lo at +32..63
 #pragma unroll

@@ -65,6 +65,15 @@ def test_prefill_workloads_full_size(dev, kind):
     assert_parity(got, ref, kind)
 
 
+def test_prefill_llama7b_bf16_full_size(dev):
+    case = workloads.make_prefill_workload("prefill_llama7b", dtype="bf16")
+    got, flags = run_prefill(case, dev)
+    assert flags == 0
+    ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
+                         case.context_lens, case.query_start, case.scale, dtype="bf16")
+    assert_parity(got, ref, "prefill_llama7b bf16", dtype="bf16")
+
+
 def test_prefill_bad_query_count_is_reported(dev):
     import paged_kv_cache_269_gb300 as pa
     case = workloads.build_prefill_case("pf_bad", [40, 40], [40, 40], num_heads=2, head_dim=128,

@@ -153,6 +153,24 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, lib=None):
     return kc, vc
 
 
+def reshape_and_cache_into(k, v, k_cache, v_cache, slot_mapping, lib=None):
+    """Store each new token's K/V at its slot in the given caches, in place
+    (C-contiguous arrays of the 16-bit element type).  Same C routine as
+    reshape_and_cache, without the copies: for timing the oracle."""
+    lib = lib or _get()
+    T, H, D = k.shape
+    N, H2, B, D2 = k_cache.shape
+    if (H2, D2) != (H, D) or v.shape != k.shape or v_cache.shape != k_cache.shape:
+        raise OracleError("shape mismatch")
+    if not (k_cache.flags.c_contiguous and v_cache.flags.c_contiguous):
+        raise OracleError("caches must be C-contiguous")
+    kk, vv, ss = _u16(k), _u16(v), _i32(slot_mapping)
+    kcu, vcu = _u16(k_cache), _u16(v_cache)
+    rc = lib.oracle_reshape_and_cache(kk[1], vv[1], kcu[1], vcu[1], ss[1], T, H, D, B, N)
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, str(rc)))
+
+
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
             lib=None, dtype: str = "f16") -> np.ndarray:
     """fp64 causal attention output [total_q, H, D]: sequence s's queries are

@@ -33,7 +33,10 @@
 //    fp32, where x is the score in the log2 domain and m a running maximum
 //    that is only raised when a tile's maximum exceeds it by more than 8 (so
 //    weights stay below 2^14, inside fp16's range); raising it rescales O_t
-//    in tensor memory once the previous P V product is done.  The weights go
+//    in tensor memory once the previous P V product is done.  The weights are
+//    first taken against the running maximum; only when a row sum exceeds
+//    2^14 (always on a query tile's first key tile) are the scores read again
+//    and the tile's maximum found first.  The weights go
 //    back into the same tensor-memory columns as a 16-bit pair P_hi + P_lo
 //    (P_hi the weight rounded to the format, P_lo the rounded remainder),
 //    which carries about 22 bits, so small outputs meet the same relative

@@ -466,19 +466,17 @@ def run_native(args, rank, world, local_rank):
         eager_s = timed(e2e_step)
         # the same step through the package's graph-replayed step runner: one
         # graph launch per step holds the host-to-device copy of the packed
-        # inputs, reshape_and_cache and decode; the output is read back after
+        # inputs, reshape_and_cache, decode and the copy of the output into
+        # pinned host memory
         from paged_kv_cache_269_gb300.step import DecodeStep
         runner = DecodeStep(d["k_cache"], d["v_cache"], case.num_seqs, case.max_blocks_per_seq,
                             case.scale, use_graph=True, partition_tokens=args.partition_tokens,
-                            stream=stream)
+                            stream=stream, host_out=True)
         runner.prepare(case.q, case.k_new, case.v_new, case.slot_mapping, case.block_tables,
                        case.context_lens)
-        out_host2 = torch.empty_like(out_host).pin_memory()
 
-        def graph_step():
-            o = runner.launch()
-            with torch.cuda.stream(stream):
-                out_host2.copy_(o, non_blocking=True)
+        def graph_step():   # one graph launch: H2D, reshape_and_cache, decode, D2H
+            runner.launch()
             stream.synchronize()
 
         graph_s = timed(graph_step)

@@ -24,7 +24,7 @@ from . import copy_blocks, decode, decode_counters_bytes, decode_workspace_bytes
 
 class DecodeStep:
     def __init__(self, k_cache, v_cache, max_seqs, max_blocks_per_seq, scale, use_graph=True,
-                 partition_tokens=0, stream=None):
+                 partition_tokens=0, stream=None, host_out=False):
         import torch
         self.torch = torch
         self.k_cache, self.v_cache = k_cache, v_cache
@@ -56,6 +56,10 @@ class DecodeStep:
         self.d = {n: self.devbuf[o:o + nb].view(td).view(shape) for n, (o, shape, nd, td, nb)
                   in self.layout.items()}
         self.out = torch.zeros((S, H, D), dtype=self.dtype, device=self.dev)
+        # with host_out, the step ends by copying the output into pinned host
+        # memory (part of the graph), read it after the stream reaches it
+        self.out_host = (torch.empty((S, H, D), dtype=self.dtype).pin_memory()
+                         if host_out else None)
         ws = decode_workspace_bytes(S, H, D, B, N, MB, partition_tokens,
                                     dtype=1 if self.dtype == torch.bfloat16 else 0)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
@@ -90,6 +94,8 @@ class DecodeStep:
         decode(self.out, d["q"], self.k_cache, self.v_cache, d["tables"], d["lens"], self.scale,
                partition_tokens=self.partition_tokens, workspace=self.workspace,
                counters=self.counters)
+        if self.out_host is not None:
+            self.out_host.copy_(self.out, non_blocking=True)
 
     def copy_on_write(self, pairs):
         """Make the manager's copy-on-write copies ((src, dst) rows) before the step."""
@@ -101,12 +107,13 @@ class DecodeStep:
 
     def launch(self):
         """Enqueue the staged step on self.stream; returns the output tensor
-        (valid once the stream reaches this point)."""
+        (valid once the stream reaches this point) -- the pinned host copy
+        when the step was built with host_out."""
         torch = self.torch
         if not self.use_graph:
             with torch.cuda.stream(self.stream):
                 self._body()
-            return self.out
+            return self.out if self.out_host is None else self.out_host
         if self.graph is None:
             with torch.cuda.stream(self.stream):
                 self._body()                        # warm-up: kernels set up outside capture
@@ -116,4 +123,4 @@ class DecodeStep:
                 self._body()
         with torch.cuda.stream(self.stream):
             self.graph.replay()
-        return self.out
+        return self.out if self.out_host is None else self.out_host

@@ -35,8 +35,8 @@ def _normal(rng, shape):
     return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
 
 
-@pytest.mark.parametrize("use_graph", [False, True])
-def test_continuous_batching_loop(dev, use_graph):
+@pytest.mark.parametrize("use_graph,host_out", [(False, False), (True, False), (True, True)])
+def test_continuous_batching_loop(dev, use_graph, host_out):
     import torch
     import paged_kv_cache_269_gb300 as pa
     from paged_kv_cache_269_gb300.step import DecodeStep
@@ -47,7 +47,8 @@ def test_continuous_batching_loop(dev, use_graph):
     kc = torch.from_numpy(mirror_k).to(dev)
     vc = torch.from_numpy(mirror_v).to(dev)
     scale = float(np.float32(1 / np.sqrt(D)))
-    step = DecodeStep(kc, vc, SMAX, MB, scale, use_graph=use_graph, partition_tokens=64)
+    step = DecodeStep(kc, vc, SMAX, MB, scale, use_graph=use_graph, partition_tokens=64,
+                      host_out=host_out)
 
     def write(slots, k, v):
         """Store token K/V at slots on the device and in the mirror."""
@@ -107,6 +108,7 @@ def test_continuous_batching_loop(dev, use_graph):
         step.prepare(q, kn, vn, np.asarray(slots, np.int32), tables, lens)
         out = step.launch()
         step.stream.synchronize()
+        assert out.is_cuda != host_out              # the pinned host copy with host_out
         got = out[:n].cpu().numpy()
         mirror_k, mirror_v = oracle.reshape_and_cache(kn, vn, mirror_k, mirror_v,
                                                       np.asarray(slots, np.int32))

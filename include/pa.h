@@ -203,7 +203,8 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  * attends to keys 0 .. p.  Built for head_dim 128, block_size 16, fp16 or
  * bf16 (PA_ERR_UNSUPPORTED otherwise).  Scores and softmax are fp32; the
  * probabilities enter the P V product as a pair of 16-bit values (P_hi +
- * P_lo) so the product keeps about 21 bits.  A sequence with q_len_s >
+ * P_lo, P_hi the weight rounded to 16 bits and P_lo the rounded remainder) so
+ * the product keeps about 22 bits.  A sequence with q_len_s >
  * ctx_s, ctx_s > max_blocks_per_seq * B, or rows outside
  * [0, total_query_tokens) is skipped and flags PA_DEVERR_CONTEXT.
  *

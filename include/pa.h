@@ -206,7 +206,9 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
  * P_lo, P_hi the weight rounded to 16 bits and P_lo the rounded remainder) so
  * the product keeps about 22 bits.  A sequence with q_len_s >
  * ctx_s, ctx_s > max_blocks_per_seq * B, or rows outside
- * [0, total_query_tokens) is skipped and flags PA_DEVERR_CONTEXT.
+ * [0, total_query_tokens) is skipped and flags PA_DEVERR_CONTEXT; so does a
+ * q_len_s above max_query_len rounded up to 256 (its rows past that are not
+ * computed).
  *
  * The kernel is persistent (one CTA per SM) and takes its work items from a
  * queue in two device counters; pa_prefill allocates them stream-ordered

@@ -358,6 +358,10 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
     it.q_len = __ldg(a.query_start + it.s + 1) - it.q_first;
     it.ctx = __ldg(a.context_lens + it.s);
     it.row0 = pair * kTiles * kBM;
+    // query rows past num_pairs * 256 (max_query_len understated) would never be
+    // computed: reported once per sequence
+    if (check && it.h == 0 && it.row0 == 0 && it.q_len > a.num_pairs * kTiles * kBM)
+        atomicOr(a.err, PA_DEVERR_CONTEXT);
     if (it.q_len <= 0 || it.row0 >= it.q_len) return false;
     if (it.ctx > a.max_blocks_per_seq * kB || it.q_len > it.ctx || it.q_first < 0 ||
         it.q_first + it.q_len > a.total_q) {

@@ -172,3 +172,23 @@ def test_prefill_bad_table_entry_is_reported(dev):
     ref = oracle.prefill(ok.q, ok.k_cache, ok.v_cache, ok.block_tables, ok.context_lens,
                          ok.query_start, ok.scale)
     assert_parity(got, ref, "prefill after a reported error")
+
+
+def test_prefill_understated_max_query_len_is_reported(dev):
+    """Rows past max_query_len (rounded up to 256) cannot be computed: the
+    call flags it; the rows below are still exact."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    case = workloads.build_prefill_case("pf_maxq", [600, 100], [600, 100], num_heads=2,
+                                        head_dim=128, seed=90)
+    d = upload(case, dev)
+    qs = torch.from_numpy(case.query_start).to(dev)
+    out = torch.full(case.q.shape, float("nan"), dtype=torch.float16, device=dev)
+    pa.prefill(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"], qs,
+               case.scale, max_query_len=200)          # pairs of 256 rows: only one
+    assert pa.device_errors() & pa.DEVERR_CONTEXT
+    got = to_numpy(out, case)
+    ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+                         case.query_start, case.scale)
+    rows = np.r_[0:256, 600:700]                     # pair 0 of both sequences
+    assert_parity(got[rows], ref[rows], "rows inside the stated bound")

@@ -47,7 +47,8 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--op", choices=["step", "copy_blocks", "swap_out", "swap_in", "prefill"],
+    p.add_argument("--op", choices=["step", "copy_blocks", "swap_out", "swap_in", "prefill",
+                                    "shared_prefix"],
                    default="step",
                    help="step: reshape_and_cache + decode (the hot path); the others time "
                         "pa_copy_blocks on a 4096-block pool, 2048 random pairs")
@@ -663,6 +664,126 @@ def run_prefill_op(args, local_rank):
         "gpu_launches": args.steps}))
 
 
+def run_shared_prefix_op(args, local_rank):
+    """Time pa_decode_shared_prefix (the tensor-core prefix kernel, then the
+    suffix decode) against pa_decode on the same 128-sequence batch sharing a
+    512-token prompt, with L2 flushed before every call (so the prefix comes
+    from HBM once per call, not from the last call's L2 lines)."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.lib()
+    case = workloads.make_workload("shared_prefix", dtype=args.dtype)
+    et = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+
+    def t(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    q, kc, vc = t(case.q), t(case.k_cache), t(case.v_cache)
+    bt, cl = t(case.block_tables), t(case.context_lens)
+    S = case.num_seqs
+    gs = torch.tensor([0, S], dtype=torch.int32, device=dev)
+    gp = torch.tensor([case.shared_prefix_blocks], dtype=torch.int32, device=dev)
+    out_s = torch.empty(case.q.shape, dtype=et, device=dev)
+    out_p = torch.empty_like(out_s)
+    stream = torch.cuda.Stream(dev)
+    dt = 1 if args.dtype == "bf16" else 0
+    dims = pa.Dims(S, case.num_heads, case.head_dim, case.block_size, case.num_blocks, dt)
+    import ctypes
+    l = pa.lib()
+    ws = torch.empty(l.pa_decode_shared_prefix_workspace_bytes(ctypes.byref(dims),
+                                                               case.max_blocks_per_seq,
+                                                               args.partition_tokens),
+                     dtype=torch.uint8, device=dev)
+    ctr = torch.zeros(l.pa_decode_shared_prefix_counters_bytes(ctypes.byref(dims)) // 4,
+                      dtype=torch.int32, device=dev)
+    ws_p = torch.empty(max(16, pa.decode_workspace_bytes(S, case.num_heads, case.head_dim,
+                                                         case.block_size, case.num_blocks,
+                                                         case.max_blocks_per_seq,
+                                                         args.partition_tokens, dtype=dt)),
+                       dtype=torch.uint8, device=dev)
+    ctr_p = torch.zeros(pa.decode_counters_bytes(S, case.num_heads) // 4, dtype=torch.int32,
+                        device=dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def shared():
+        pa.decode_shared_prefix(out_s, q, kc, vc, bt, cl, case.scale, gs, gp, max_group_size=S,
+                                partition_tokens=args.partition_tokens, counters=ctr,
+                                workspace=ws, stream=stream)
+
+    def plain():
+        pa.decode(out_p, q, kc, vc, bt, cl, case.scale, partition_tokens=args.partition_tokens,
+                  workspace=ws_p, counters=ctr_p, stream=stream)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e0, e1 in evs:
+            with torch.cuda.stream(stream):
+                flush_buf.fill_(1)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    sampler = ClockSampler(local_rank) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t_begin = time.time()
+    ms_s = timed(shared)
+    ms_p = timed(plain)
+    t_end = time.time()
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+    if pa.device_errors(stream=stream):
+        raise RuntimeError("device error during the timed calls")
+    # two correct answers (within the decode tolerance of the oracle, which the
+    # tests check): here only that they agree with each other
+    diff = float((out_s.float() - out_p.float()).abs().max())
+    if not diff <= 4e-3:
+        raise RuntimeError(f"shared-prefix and plain decode disagree by {diff}")
+    shared_ms = sum(ms_s) / len(ms_s)
+    plain_ms = sum(ms_p) / len(ms_p)
+    uniq = workloads.decode_unique_bytes(case)
+    logical = workloads.decode_algorithmic_bytes(case)
+    peak, peak_kind = measured_peaks()
+    achieved = uniq / (shared_ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "shared-prefix decode GB/s (unique bytes)", "value": round(achieved, 2),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(shared_ms, 4), "higher_is_better": True, "dtype": args.dtype,
+        "data": "synthetic",
+        "config": {"workload": "shared_prefix", "num_seqs": S, "num_heads": case.num_heads,
+                   "head_dim": case.head_dim, "prefix_blocks": case.shared_prefix_blocks,
+                   "total_context_tokens": int(case.context_lens.sum()),
+                   "partition_tokens": args.partition_tokens or 512,
+                   "l2": "flushed before every call (256 MiB write, outside the events)"},
+        "ms_median": round(statistics.median(ms_s), 4),
+        "plain_decode_ms": round(plain_ms, 4),
+        "plain_decode_unique_gbs": round(uniq / (plain_ms * 1e-3) / 1e9, 2),
+        "speedup_vs_plain": round(plain_ms / shared_ms, 3),
+        "logical_gbs": round(logical / (shared_ms * 1e-3) / 1e9, 2),
+        "tokens_per_s": round(S / (shared_ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "prefix kernel + suffix decode (two launches)",
+                     "unique_bytes_per_call": int(uniq), "logical_bytes_per_call": int(logical),
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(t_begin, t_end) if sampler else None}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -674,6 +795,10 @@ def main():
     if args.op == "prefill":
         if rank == 0:
             run_prefill_op(args, local_rank)
+        return
+    if args.op == "shared_prefix":
+        if rank == 0:
+            run_shared_prefix_op(args, local_rank)
         return
     if args.op != "step":
         if rank == 0:

@@ -55,6 +55,8 @@ typedef enum pa_status {
 #define PA_DEVERR_CONTEXT 0x2u  /* a context length was < 0 or > max_blocks_per_seq * block_size */
 #define PA_DEVERR_SLOT    0x4u  /* a slot_mapping entry was >= num_blocks * block_size      */
 #define PA_DEVERR_TIMEOUT 0x8u  /* an internal pipeline wait gave up (should never happen) */
+#define PA_DEVERR_PREFIX  0x10u /* pa_decode_shared_prefix: a sequence could not use its group's
+                                   shared prefix (see there) and was decoded in full instead */
 
 /* Element type of q, the caches and the output (and of k, v for
  * reshape_and_cache): IEEE binary16, or bfloat16 (the top 16 bits of an
@@ -281,6 +283,83 @@ int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_ca
                  int32_t max_blocks_per_seq, const pa_dims *dims, int32_t partition_tokens,
                  void *workspace, size_t workspace_bytes, uint32_t *counters,
                  size_t counters_bytes, void *stream);
+
+/*
+ * pa_decode_shared_prefix_ws -- pa_decode for a batch in which groups of
+ * sequences share the first blocks of their block tables: a common system
+ * prompt, or several samples forked from one prompt ("vLLM 2026
+ * 推理引擎全解", §2.3: the shared prefix is stored once and referenced by every
+ * request; doramagic.ai vLLM manual, "共享机制").  The output is that of
+ * pa_decode (within the decode tolerance); what changes is the work.  The
+ * pages share the prefix's memory; this call also shares its reads: the
+ * prefix's K/V are read once per group and head instead of once per sequence.
+ *
+ *   out, q, k_cache, v_cache, block_tables, context_lens, scale,
+ *   max_blocks_per_seq, dims, partition_tokens: as pa_decode_ws
+ *   group_start          device, int32 [num_groups + 1], non-decreasing
+ *                        within [0, S]: group g is the sequences
+ *                        group_start[g] .. group_start[g + 1] - 1 (sequences
+ *                        outside every group are decoded as by pa_decode)
+ *   group_prefix_blocks  device, int32 [num_groups]: P_g, the number of
+ *                        leading block-table entries every sequence of group g
+ *                        shares with the group's first sequence (0: none)
+ *   num_groups           host, >= 0
+ *   max_group_size       host: an upper bound of the group sizes (sizes the
+ *                        prefix work)
+ *   workspace            device, pa_decode_shared_prefix_workspace_bytes(...)
+ *                        bytes (never 0), 16-byte aligned, no initialisation
+ *   counters             device, pa_decode_shared_prefix_counters_bytes(dims)
+ *                        bytes, 4-byte aligned, all zero before the first call
+ *                        and left zero by every call that completes without a
+ *                        device error (as pa_decode_ws)
+ *
+ * Two launches on `stream` (when num_groups or max_group_size is 0, only
+ * pa_decode's):
+ *  1. The tcgen05 prefill kernel, in a non-causal mode: for each group, head
+ *     and tile of up to 128 member queries, S = Q K^T and P V over the
+ *     group's P_g * B prefix keys (read through the group's first sequence's
+ *     table), written as one partial result -- (max, sum) and the
+ *     unnormalised output -- per member and head.
+ *  2. The decode kernel: each member's blocks P_g .. ceil(ctx_s / B) - 1,
+ *     merged with the prefix partial by the split-context combine.  It
+ *     starts while the prefill kernel still runs (programmatic dependent
+ *     launch; that kernel waited for the inputs before letting it start) and
+ *     waits for it only before the merges that read a prefix partial, which
+ *     each warp makes after its last work unit.
+ *
+ * A member is decoded in full, as by pa_decode, and PA_DEVERR_PREFIX is set,
+ * when its first P_g table entries differ from the group's first sequence's,
+ * its context is shorter than P_g * B, it lies past max_group_size rounded up
+ * to 256 within its group, or the group arrays are malformed (decreasing,
+ * outside [0, S], or P_g outside [0, max_blocks_per_seq]).  Outputs are
+ * therefore always those of pa_decode; the flag reports the wasted work.
+ *
+ * Built for head_dim 128 and block_size 16, fp16 or bf16 (the prefill
+ * kernel's shapes); PA_ERR_UNSUPPORTED otherwise.  The prefix keys enter
+ * P V as a 16-bit pair (about 22 bits), as in pa_prefill.
+ */
+size_t pa_decode_shared_prefix_workspace_bytes(const pa_dims *dims, int32_t max_blocks_per_seq,
+                                               int32_t partition_tokens);
+size_t pa_decode_shared_prefix_counters_bytes(const pa_dims *dims);
+int pa_decode_shared_prefix_ws(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               float scale, int32_t max_blocks_per_seq, const pa_dims *dims,
+                               const int32_t *group_start, const int32_t *group_prefix_blocks,
+                               int32_t num_groups, int32_t max_group_size,
+                               int32_t partition_tokens, void *workspace, size_t workspace_bytes,
+                               uint32_t *counters, size_t counters_bytes, void *stream);
+
+/*
+ * pa_decode_shared_prefix -- pa_decode_shared_prefix_ws with its counters and
+ * workspace allocated stream-ordered (cudaMallocAsync / cudaFreeAsync, the
+ * counters zeroed with cudaMemsetAsync) for the call, and the default
+ * partition length.
+ */
+int pa_decode_shared_prefix(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens, float scale,
+                            int32_t max_blocks_per_seq, const pa_dims *dims,
+                            const int32_t *group_start, const int32_t *group_prefix_blocks,
+                            int32_t num_groups, int32_t max_group_size, void *stream);
 
 /* Capacity of the scratch array pa_decode_static uses instead of allocating. */
 #define PA_STATIC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB per device */

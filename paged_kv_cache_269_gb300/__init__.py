@@ -11,6 +11,8 @@ Functions (names follow the C ABI):
   reshape_and_cache(k, v, k_cache, v_cache, slot_mapping)
   copy_blocks(src_k, src_v, dst_k, dst_v, block_pairs)
   decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, ...)
+  decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                       group_start, group_prefix_blocks, ...)
   decode_workspace_bytes(...), decode_counters_bytes(...), device_errors(), version(),
   selftest_wait_timeout()
 """
@@ -22,15 +24,16 @@ import threading
 from . import build as _build
 
 __all__ = ["PaError", "Dims", "KVManager", "lib", "reshape_and_cache", "copy_blocks", "decode",
-           "selftest_wait_timeout",
+           "decode_shared_prefix", "selftest_wait_timeout",
            "prefill", "decode_workspace_bytes",
            "decode_counters_bytes", "device_errors", "reset_workspaces", "version", "DEVERR_TABLE", "DEVERR_CONTEXT",
-           "DEVERR_SLOT", "DEVERR_TIMEOUT"]
+           "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_PREFIX"]
 
 DEVERR_TABLE = 0x1
 DEVERR_CONTEXT = 0x2
 DEVERR_SLOT = 0x4
 DEVERR_TIMEOUT = 0x8
+DEVERR_PREFIX = 0x10
 
 STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_UNSUPPORTED",
           -4: "PA_ERR_ALIGN", -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_CUDA",
@@ -43,7 +46,9 @@ EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", 
            "pa_status_string", "pa_last_cuda_error", "pa_version",
            "pa_kvm_create", "pa_kvm_destroy", "pa_kvm_num_free_blocks", "pa_kvm_refcount",
            "pa_kvm_add_sequence", "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free",
-           "pa_kvm_context_len", "pa_kvm_slot", "pa_kvm_block_tables", "pa_selftest_wait_timeout")
+           "pa_kvm_context_len", "pa_kvm_slot", "pa_kvm_block_tables", "pa_selftest_wait_timeout",
+           "pa_decode_shared_prefix", "pa_decode_shared_prefix_ws",
+           "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix_counters_bytes")
 _SIZE_ERROR = (1 << 64) - 1
 
 
@@ -85,6 +90,14 @@ def _declare(l):
     l.pa_decode_ws.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, i32, vp, sz, vp,
                                sz, vp]
     l.pa_decode_static.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp]
+    l.pa_decode_shared_prefix_workspace_bytes.argtypes = [dp, i32, i32]
+    l.pa_decode_shared_prefix_workspace_bytes.restype = sz
+    l.pa_decode_shared_prefix_counters_bytes.argtypes = [dp]
+    l.pa_decode_shared_prefix_counters_bytes.restype = sz
+    l.pa_decode_shared_prefix_ws.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp, vp,
+                                             i32, i32, i32, vp, sz, vp, sz, vp]
+    l.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, dp, vp, vp,
+                                          i32, i32, vp]
     l.pa_decode_static.restype = ctypes.c_int
     l.pa_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     l.pa_status_string.argtypes = [ctypes.c_int]
@@ -110,7 +123,7 @@ def _declare(l):
                  "pa_kvm_slot", "pa_kvm_block_tables"):
         getattr(l, name).restype = i32
     for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", "pa_prefill_ws",
-                 "pa_decode_ws",
+                 "pa_decode_ws", "pa_decode_shared_prefix", "pa_decode_shared_prefix_ws",
                  "pa_device_errors",
                  "pa_last_cuda_error", "pa_version"):
         getattr(l, name).restype = ctypes.c_int
@@ -426,6 +439,75 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                             int(partition_tokens), ws_ptr, ws_n, _ptr(counters),
                             counters.numel() * 4, sh)
     _check(rc, "pa_decode_ws")
+    return out
+
+
+def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                         group_start, group_prefix_blocks, max_group_size=None,
+                         partition_tokens=0, workspace=None, counters=None, stream=None,
+                         allocate_in_library=False):
+    """decode() for a batch whose sequences form groups sharing the first
+    blocks of their tables (pa_decode_shared_prefix_ws; pa_decode_shared_prefix
+    with allocate_in_library).  group_start [G + 1] and group_prefix_blocks [G]
+    are int32 CUDA tensors: group g is sequences group_start[g] ..
+    group_start[g + 1] - 1, sharing their first group_prefix_blocks[g] table
+    entries.  max_group_size bounds the group sizes (computed from
+    group_start, with a device sync, when None).  The output equals decode()'s;
+    a sequence that does not really share its group's prefix is decoded in
+    full and flags DEVERR_PREFIX.  counters / workspace: as decode(), sized by
+    the shared-prefix byte counts; by default cached per-stream buffers."""
+    torch = _torch()
+    _element_dtype(k_cache)
+    et = k_cache.dtype
+    _need(k_cache, "k_cache", et, 4)
+    dev = k_cache.device
+    _need(v_cache, "v_cache", et, 4, dev)
+    _need(q, "q", et, 3, dev)
+    _need(out, "out", et, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    _need(group_start, "group_start", torch.int32, 1, dev)
+    _need(group_prefix_blocks, "group_prefix_blocks", torch.int32, 1, dev)
+    N, H, B, D = k_cache.shape
+    S = q.shape[0]
+    G = group_prefix_blocks.shape[0]
+    if v_cache.shape != k_cache.shape or q.shape != (S, H, D) or out.shape != q.shape \
+            or block_tables.shape[0] != S or context_lens.shape[0] != S \
+            or group_start.shape[0] != G + 1:
+        raise ValueError("decode_shared_prefix: inconsistent shapes")
+    if max_group_size is None:
+        max_group_size = int((group_start[1:] - group_start[:-1]).max()) if G else 0
+    MB = block_tables.shape[1]
+    dims = _cache_dims(k_cache, S)
+    sh, st = _stream_handle(dev, stream)
+    l = lib()
+    with torch.cuda.device(dev):
+        if allocate_in_library:
+            rc = l.pa_decode_shared_prefix(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(block_tables), _ptr(context_lens), float(scale),
+                                           MB, ctypes.byref(dims), _ptr(group_start),
+                                           _ptr(group_prefix_blocks), G, int(max_group_size), sh)
+            _check(rc, "pa_decode_shared_prefix")
+            return out
+        need_ws = l.pa_decode_shared_prefix_workspace_bytes(ctypes.byref(dims), MB,
+                                                            int(partition_tokens))
+        need_ctr = l.pa_decode_shared_prefix_counters_bytes(ctypes.byref(dims))
+        if need_ws == _SIZE_ERROR or need_ctr == 0:
+            raise PaError(-2, "decode_shared_prefix: invalid sizes")
+        if counters is None or workspace is None:
+            c2, w2 = _buffers_for(dev, st, need_ctr, need_ws)
+            counters = c2 if counters is None else counters
+            workspace = w2 if workspace is None else workspace
+        _need(counters, "counters", torch.int32, 1, dev)
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+        rc = l.pa_decode_shared_prefix_ws(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(block_tables), _ptr(context_lens), float(scale),
+                                          MB, ctypes.byref(dims), _ptr(group_start),
+                                          _ptr(group_prefix_blocks), G, int(max_group_size),
+                                          int(partition_tokens), _ptr(workspace),
+                                          workspace.numel(), _ptr(counters),
+                                          counters.numel() * 4, sh)
+    _check(rc, "pa_decode_shared_prefix_ws")
     return out
 
 

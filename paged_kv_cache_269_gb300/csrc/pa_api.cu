@@ -120,6 +120,31 @@ int check_device_addressable(const void *p, int device) {
     }
 }
 
+// Buffers of a shared-prefix decode.  Counters (zero on entry and exit):
+// the decode kernel's, then the prefix kernel's two (in 256 bytes).
+// Workspace (no initialisation): the decode partials with one more slot per
+// (sequence, head), slot 0, for the prefix partial.
+struct SharedLayout {
+    WorkspaceLayout dec;
+    int32_t tiles_per_unit, max_parts;
+    size_t prefix_counters_off, counters_bytes, workspace_bytes;
+};
+
+int shared_layout(const pa_dims *dims, int32_t max_blocks_per_seq, int32_t partition_tokens,
+                  SharedLayout *out) {
+    SharedLayout l;
+    int rc = partition_plan(dims, max_blocks_per_seq, partition_tokens, &l.tiles_per_unit,
+                            &l.max_parts);
+    if (rc != PA_OK) return rc;
+    l.max_parts += 1;
+    workspace_layout(dims->num_seqs, dims->num_heads, dims->head_dim, l.max_parts, &l.dec);
+    l.prefix_counters_off = l.dec.counters_bytes;
+    l.counters_bytes = l.prefix_counters_off + 256;
+    l.workspace_bytes = l.dec.workspace_bytes;
+    *out = l;
+    return PA_OK;
+}
+
 }  // namespace
 
 int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
@@ -252,6 +277,10 @@ int pa_prefill_ws(void *out, const void *q, const void *k_cache, const void *v_c
     a.num_pairs = static_cast<int32_t>(pairs);
     a.counters = counters;
     a.err = err;
+    a.group_prefix_blocks = nullptr;
+    a.part_ml = nullptr;
+    a.part_acc = nullptr;
+    a.max_parts = 0;
     const cudaError_t e = launch_prefill(a, q, k_cache, v_cache, dims->dtype, sms,
                                          static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;  // tensor maps could not be made
@@ -348,6 +377,10 @@ int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_ca
     a.part_ml = parts > 1 ? reinterpret_cast<float *>(ws + l.ml_off) : nullptr;
     a.part_acc = parts > 1 ? reinterpret_cast<float *>(ws + l.acc_off) : nullptr;
     a.err = st->err;
+    a.group_start = nullptr;
+    a.group_prefix_blocks = nullptr;
+    a.num_groups = 0;
+    a.rows_cap = 0;
     cudaError_t e = launch_decode(a, dims->dtype, dims->head_dim, dims->block_size, st->num_sms,
                                   static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidConfiguration) return PA_ERR_UNSUPPORTED;  // too many sequences
@@ -384,6 +417,153 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
                       max_blocks_per_seq, dims, 0, l.workspace_bytes ? base + l.counters_bytes : nullptr,
                       l.workspace_bytes, reinterpret_cast<uint32_t *>(base), l.counters_bytes,
                       stream);
+    e = cudaFreeAsync(buf, s);
+    if (rc != PA_OK) return rc;
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+size_t pa_decode_shared_prefix_workspace_bytes(const pa_dims *dims, int32_t max_blocks_per_seq,
+                                               int32_t partition_tokens) {
+    if (check_dims(dims, true) != PA_OK) return static_cast<size_t>(-1);
+    SharedLayout l;
+    if (shared_layout(dims, max_blocks_per_seq, partition_tokens, &l) != PA_OK)
+        return static_cast<size_t>(-1);
+    return l.workspace_bytes;
+}
+
+size_t pa_decode_shared_prefix_counters_bytes(const pa_dims *dims) {
+    if (check_dims(dims, true) != PA_OK) return 0;
+    SharedLayout l;
+    if (shared_layout(dims, 1, 0, &l) != PA_OK) return 0;
+    return l.counters_bytes;
+}
+
+int pa_decode_shared_prefix_ws(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               float scale, int32_t max_blocks_per_seq, const pa_dims *dims,
+                               const int32_t *group_start, const int32_t *group_prefix_blocks,
+                               int32_t num_groups, int32_t max_group_size,
+                               int32_t partition_tokens, void *workspace, size_t workspace_bytes,
+                               uint32_t *counters, size_t counters_bytes, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != PA_OK) return rc;
+    if (!prefill_supported(dims->dtype, dims->head_dim, dims->block_size)) return PA_ERR_UNSUPPORTED;
+    if (num_groups < 0 || max_group_size < 0) return PA_ERR_SHAPE;
+    SharedLayout l;
+    rc = shared_layout(dims, max_blocks_per_seq, partition_tokens, &l);
+    if (rc != PA_OK) return rc;
+    if (dims->num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
+    const bool groups = num_groups > 0 && max_group_size > 0;
+    if (groups && (!group_start || !group_prefix_blocks)) return PA_ERR_NULL;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PA_ERR_ALIGN;
+    if (!isfinite(scale)) return PA_ERR_SHAPE;
+    // the prefix kernel's tensor-map coordinates and work items are 32-bit
+    const long long pairs = (static_cast<long long>(max_group_size) + 255) / 256;
+    if (static_cast<long long>(dims->num_blocks) * dims->num_heads * dims->block_size > 0x7fffffffLL ||
+        pairs * num_groups * dims->num_heads > 0x7fffffffLL)
+        return PA_ERR_SHAPE;
+    if (!counters || counters_bytes < l.counters_bytes || !aligned(counters, 4))
+        return PA_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < l.workspace_bytes || !aligned(workspace, 16))
+        return PA_ERR_WORKSPACE;
+
+    DeviceState *st = nullptr;
+    rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    // checked before the prefix kernel writes anything into the counters
+    if (!decode_fits(dims->dtype, dims->head_dim, dims->block_size, dims->num_seqs,
+                     groups ? num_groups : -1))
+        return PA_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *ctr = reinterpret_cast<uint8_t *>(counters);
+    float *part_ml = reinterpret_cast<float *>(ws + l.dec.ml_off);
+    float *part_acc = reinterpret_cast<float *>(ws + l.dec.acc_off);
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+    if (groups) {
+        PrefillArgs p;
+        p.out = nullptr;
+        p.block_tables = block_tables;
+        p.context_lens = context_lens;
+        p.query_start = group_start;
+        p.scale_log2 = scale_log2;
+        p.num_seqs = num_groups;
+        p.num_heads = dims->num_heads;
+        p.num_blocks = dims->num_blocks;
+        p.max_blocks_per_seq = max_blocks_per_seq;
+        p.total_q = dims->num_seqs;
+        p.num_pairs = static_cast<int32_t>(pairs);
+        p.counters = reinterpret_cast<uint32_t *>(ctr + l.prefix_counters_off);
+        p.err = st->err;
+        p.group_prefix_blocks = group_prefix_blocks;
+        p.part_ml = part_ml;
+        p.part_acc = part_acc;
+        p.max_parts = l.max_parts;
+        const cudaError_t e = launch_prefill(p, q, k_cache, v_cache, dims->dtype, st->num_sms, s);
+        if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;  // tensor maps could not be made
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    DecodeArgs a;
+    a.out = static_cast<uint16_t *>(out);
+    a.q = static_cast<const uint16_t *>(q);
+    a.k_cache = static_cast<const uint16_t *>(k_cache);
+    a.v_cache = static_cast<const uint16_t *>(v_cache);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.scale_log2 = scale_log2;
+    a.num_seqs = dims->num_seqs;
+    a.num_heads = dims->num_heads;
+    a.num_blocks = dims->num_blocks;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.tiles_per_unit = l.tiles_per_unit;
+    a.max_parts = l.max_parts;
+    a.counters = counters;
+    a.part_ml = part_ml;
+    a.part_acc = part_acc;
+    a.err = st->err;
+    a.group_start = groups ? group_start : nullptr;
+    a.group_prefix_blocks = groups ? group_prefix_blocks : nullptr;
+    a.num_groups = groups ? num_groups : 0;
+    a.rows_cap = static_cast<int32_t>(pairs * 256 > 0x7fffffffLL ? 0x7fffffffLL : pairs * 256);
+    const cudaError_t e = launch_decode(a, dims->dtype, dims->head_dim, dims->block_size,
+                                        st->num_sms, s);
+    if (e == cudaErrorInvalidConfiguration) return PA_ERR_UNSUPPORTED;  // too many sequences
+    return e == cudaSuccess ? PA_OK : fail_cuda(e);
+}
+
+int pa_decode_shared_prefix(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens, float scale,
+                            int32_t max_blocks_per_seq, const pa_dims *dims,
+                            const int32_t *group_start, const int32_t *group_prefix_blocks,
+                            int32_t num_groups, int32_t max_group_size, void *stream) {
+    int rc = check_dims(dims, true);
+    if (rc != PA_OK) return rc;
+    if (!prefill_supported(dims->dtype, dims->head_dim, dims->block_size)) return PA_ERR_UNSUPPORTED;
+    SharedLayout l;
+    rc = shared_layout(dims, max_blocks_per_seq, 0, &l);
+    if (rc != PA_OK) return rc;
+    if (dims->num_seqs == 0) return PA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceState *st = nullptr;
+    rc = current_device_state(&st);
+    if (rc != PA_OK) return rc;
+    void *buf = nullptr;
+    cudaError_t e = cudaMallocAsync(&buf, l.counters_bytes + l.workspace_bytes, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = cudaMemsetAsync(buf, 0, l.counters_bytes, s);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(buf, s);
+        return fail_cuda(e);
+    }
+    uint8_t *base = static_cast<uint8_t *>(buf);
+    rc = pa_decode_shared_prefix_ws(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                    max_blocks_per_seq, dims, group_start, group_prefix_blocks,
+                                    num_groups, max_group_size, 0, base + l.counters_bytes,
+                                    l.workspace_bytes, reinterpret_cast<uint32_t *>(base),
+                                    l.counters_bytes, stream);
     e = cudaFreeAsync(buf, s);
     if (rc != PA_OK) return rc;
     return e == cudaSuccess ? PA_OK : fail_cuda(e);

@@ -97,15 +97,28 @@ struct Cfg {
     static constexpr int OFF_BARS = (OFF_STAGE_TAG + NS * 4 + 7) / 8 * 8;
     static constexpr int NUM_BARS = 2 * NS + 3 * ND;
     static constexpr int OFF_FLAGS = OFF_BARS + NUM_BARS * 8;
-    static constexpr int OFF_SEQ = OFF_FLAGS + 16;    // prefix[S + 1], ctx[S]
+    static constexpr int OFF_SEQ = OFF_FLAGS + 16;    // prefix[S + 1], ctx[S] (+ shared-prefix state)
+    static constexpr int DEFER = 8;                   // deferred prefix merges per consumer warp
+    static constexpr int KEYS = 32;                   // unit-length classes of the work order
 
     // CTAs per SM the shared-memory footprint allows (228 KiB per SM, 1 KiB
     // reserved per CTA, room for 1024 sequences); the launch bound caps the
     // registers so that as many CTAs fit.
     static constexpr int MIN_BLOCKS = clamp_int(228 * 1024 / (OFF_SEQ + 8 * 1024 + 1024), 1, 8);
 
-    static size_t smem_bytes(int num_seqs) {
-        return static_cast<size_t>(OFF_SEQ) + (2 * static_cast<size_t>(num_seqs) + 1) * 4;
+    // Shared-prefix mode (num_groups >= 0) adds each sequence's first block
+    // and place in the work order, the group starts, the order's length
+    // classes, and the deferred-merge lists (kept small: at S = 128 four
+    // CTAs per SM still fit).
+    __host__ __device__ static size_t seq_ints(int num_seqs, int num_groups) {
+        const size_t S = static_cast<size_t>(num_seqs);
+        return num_groups < 0 ? 2 * S + 1
+                              : 4 * S + 1 + static_cast<size_t>(num_groups) + 1 + KEYS;
+    }
+    static size_t smem_bytes(int num_seqs, int num_groups) {
+        size_t n = static_cast<size_t>(OFF_SEQ) + seq_ints(num_seqs, num_groups) * 4;
+        if (num_groups >= 0) n = (n + 7) / 8 * 8 + static_cast<size_t>(NC) * DEFER * 8;
+        return n;
     }
 };
 
@@ -338,6 +351,35 @@ __device__ __forceinline__ void store_f32(float *dst, const float (&v)[DPL]) {
         *reinterpret_cast<float2 *>(dst + i) = make_float2(v[i], v[i + 1]);
 }
 
+// One warp: out[s, h] from partials begin .. end - 1 of (s, h) = sh in the
+// workspace, (max, sum) pairs and unnormalised outputs written by other CTAs
+// or launches (read through L2).
+template <typename E, int D, int DPL>
+__device__ __forceinline__ void combine_partials(const DecodeArgs &a, size_t sh, int begin,
+                                                 int end, int lane) {
+    const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml) + sh * a.max_parts;
+    const float *pacc = a.part_acc + sh * a.max_parts * D + lane * DPL;
+    float GM = -INFINITY;
+    for (int i = begin + lane; i < end; i += 32) GM = fmaxf(GM, __ldcg(pml + i).x);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) GM = fmaxf(GM, __shfl_xor_sync(kFull, GM, off));
+    float GL = 0.f;
+    float go[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) go[e] = 0.f;
+#pragma unroll 4
+    for (int i = begin; i < end; ++i) {
+        const float2 ml = __ldcg(pml + i);
+        float v[DPL];
+        load_f32<DPL>(pacc + static_cast<size_t>(i) * D, v, true);
+        const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - GM);
+        GL = fmaf(f, ml.y, GL);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) go[e] = fmaf(f, v[e], go[e]);
+    }
+    store_out<E, DPL>(a.out + sh * D + lane * DPL, go, GL > 0.f ? 1.f / GL : 0.f);
+}
+
 template <typename E, int D, int B>
 __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     decode_kernel(const DecodeArgs a) {
@@ -364,6 +406,18 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     const int H = a.num_heads;
     int *prefix = reinterpret_cast<int *>(smem + C::OFF_SEQ);  // [S + 1]
     int *ctx_of = prefix + S + 1;                              // [S]
+    // Shared-prefix mode.  start_of[s]: the leading blocks of s that the
+    // prefix kernel's partial (slot 0) may cover, provided s's table starts
+    // like that of its group's first sequence (the producer checks this per
+    // unit); this kernel covers the rest.
+    const bool shared = a.group_start != nullptr;
+    const int G = shared ? a.num_groups : 0;
+    int *start_of = ctx_of + S;                                // [S]
+    int *order = start_of + S;                                 // [S] work order: position -> s
+    int *gstart = order + S;                                   // [G + 1]
+    int *classes = gstart + G + 1;                             // [KEYS]
+    uint2 *defer = reinterpret_cast<uint2 *>(
+        smem + (C::OFF_SEQ + C::seq_ints(S, G) * 4 + 7) / 8 * 8);   // [NC][DEFER]
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -386,25 +440,116 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     }
     // Everything above touched shared memory only; inputs may still be being
     // written by the previous kernel on the stream (e.g. reshape_and_cache).
-    grid_dependency_wait();
+    // After the shared-prefix kernel, which waited for them before letting
+    // this one launch, only its partials are outstanding: the wait moves to
+    // where they are read (and to the end).
+    if (!shared) grid_dependency_wait();
     allow_dependents_to_launch();
     const int ctx_cap = a.max_blocks_per_seq * B;
+    bool malformed = false;
+    if (shared) {
+        // the group arrays: non-decreasing within [0, S], P_g within the table
+        for (int g = threadIdx.x; g <= G; g += blockDim.x) gstart[g] = __ldg(a.group_start + g);
+        __syncthreads();
+        bool bad = false;
+        for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+            const int lo = gstart[g];
+            bad = bad || lo < 0 || lo > S;
+            if (g < G) {
+                const int pb = __ldg(a.group_prefix_blocks + g);
+                bad = bad || gstart[g + 1] < lo || pb < 0 || pb > a.max_blocks_per_seq;
+            }
+        }
+        malformed = __syncthreads_or(bad) != 0;
+        if (malformed && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_PREFIX);
+    }
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
-        int c = a.context_lens[s];
+        const int c_in = a.context_lens[s];
+        int c = c_in;
         if (c < 0 || c > ctx_cap) {
             atomicOr(a.err, PA_DEVERR_CONTEXT);
             c = c < 0 ? 0 : ctx_cap;
         }
         const int nblk = (c + B - 1) / B;
+        int first = 0;
+        if (shared) {
+            if (!malformed && G > 0 && gstart[0] <= s) {
+                int lo = 0, hi = G - 1;   // the last group starting at or before s
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (gstart[mid] <= s) lo = mid; else hi = mid - 1;
+                }
+                const int pb = __ldg(a.group_prefix_blocks + lo);
+                if (s < gstart[lo + 1] && pb > 0) {
+                    // rows the prefix kernel covers, whose context holds the prefix
+                    if (c_in >= pb * B && c_in <= ctx_cap && s - gstart[lo] < a.rows_cap) {
+                        first = pb;
+                    } else if (blockIdx.x == 0) {
+                        atomicOr(a.err, PA_DEVERR_PREFIX);
+                    }
+                }
+            }
+            start_of[s] = first;
+        }
+        const int rest = nblk - first;
         ctx_of[s] = c;
-        prefix[s + 1] = nblk == 0 ? 1 : (nblk + TPU - 1) / TPU;  // partitions of s
+        if (!shared) prefix[s + 1] = rest == 0 ? 1 : (rest + TPU - 1) / TPU;  // partitions of s
     }
     __syncthreads();
-    if (warp == C::NC) {  // exclusive prefix over sequences of their partition counts
+    if (shared && warp == C::NC) {
+        // Work order, shared-prefix mode: longest first unit first (a stable
+        // counting sort, descending, over KEYS length classes), so that the
+        // queue ends on short units.  Plain decode keeps sequence order (its
+        // concurrent CTAs then share the L2 lines of common blocks); here the
+        // common blocks are the prefix kernel's.  Every CTA derives the same
+        // order: counts, then placement in sequence order within a class.
+        static_assert(C::KEYS == 32, "one length class per lane");
+        auto key_of = [&](int s) {
+            const int rest = (ctx_of[s] + B - 1) / B - start_of[s];
+            return min(rest, TPU) * (C::KEYS - 1) / TPU;
+        };
+        classes[lane] = 0;
+        __syncwarp();
+        for (int s = lane; s < S; s += 32) atomicAdd(&classes[key_of(s)], 1);
+        __syncwarp();
+        {   // first place of class k: the sizes of the classes above it
+            const int k = C::KEYS - 1 - lane;
+            const int n = classes[k];
+            int v = n;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(kFull, v, off);
+                if (lane >= off) v += y;
+            }
+            __syncwarp();
+            classes[k] = v - n;
+        }
+        __syncwarp();
+        for (int base = 0; base < S; base += 32) {
+            const int s = base + lane;
+            const unsigned active = __ballot_sync(kFull, s < S);
+            if (s < S) {
+                const int k = key_of(s);
+                const unsigned peers = __match_any_sync(active, k);
+                order[classes[k] + __popc(peers & ((1u << lane) - 1u))] = s;
+                __syncwarp(active);
+                if (lane == __ffs(peers) - 1) classes[k] += __popc(peers);
+            }
+            __syncwarp();
+        }
+    }
+    if (warp == C::NC) {  // exclusive prefix over the order of partition counts
         int running = 0;
         for (int base = 0; base < S; base += 32) {
             const int s = base + lane;
-            int v = s < S ? prefix[s + 1] : 0;
+            int v = 0;
+            if (s < S && shared) {   // partitions of the sequence in place s
+                const int r = order[s];
+                const int rest = (ctx_of[r] + B - 1) / B - start_of[r];
+                v = rest == 0 ? 1 : (rest + TPU - 1) / TPU;
+            } else if (s < S) {
+                v = prefix[s + 1];
+            }
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const int y = __shfl_up_sync(kFull, v, off);
@@ -432,18 +577,40 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
             if (lane == 0) pending = atomicAdd(&a.counters[0], 1u);  // prefetch the next grab
             const int g = static_cast<int>(u / H);
             const int h = static_cast<int>(u - static_cast<uint32_t>(g) * H);
-            int lo = 0, hi = S - 1;  // sequence s with prefix[s] <= g < prefix[s + 1]
+            int lo = 0, hi = S - 1;  // position i with prefix[i] <= g < prefix[i + 1]
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
             }
-            const int s = lo;
-            const int p = g - prefix[s];
-            const int np = prefix[s + 1] - prefix[s];
+            const int s = shared ? order[lo] : lo;
+            const int p = g - prefix[lo];
+            const int np = prefix[lo + 1] - prefix[lo];
             const int ctx = ctx_of[s];
             const int nblk = (ctx + B - 1) / B;
-            const int t0 = p * TPU;
-            const int nt = max(0, min(TPU, nblk - t0));
+            const int first = shared ? start_of[s] : 0;
+            bool pre = first > 0;
+            int leader = s;
+            if (pre) {   // the group's first sequence: the last group start at or before s
+                int glo = 0, ghi = G - 1;
+                while (glo < ghi) {
+                    const int mid = (glo + ghi + 1) >> 1;
+                    if (gstart[mid] <= s) glo = mid; else ghi = mid - 1;
+                }
+                leader = gstart[glo];
+            }
+            if (pre && leader != s) {
+                // the prefix partial is s's only if s's first blocks are its
+                // group's; otherwise the first partition takes them on
+                const int32_t *mine = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
+                const int32_t *lead =
+                    a.block_tables + static_cast<size_t>(leader) * a.max_blocks_per_seq;
+                bool same = true;
+                for (int b = lane; b < first; b += 32) same = same && __ldg(mine + b) == __ldg(lead + b);
+                pre = __all_sync(kFull, same);
+                if (!pre && lane == 0 && h == 0 && p == 0) atomicOr(a.err, PA_DEVERR_PREFIX);
+            }
+            const int t0 = (pre || p > 0) ? first + p * TPU : 0;
+            const int nt = max(0, min(nblk, first + (p + 1) * TPU) - t0);
 
             const int slot = static_cast<int>(dq % C::ND);
             bool w_ok = mbar_wait(&desc_empty[slot], ((dq / C::ND) & 1u) ^ 1u, abort_flag, a.err);
@@ -451,6 +618,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
             if (lane == 0) {
                 int *m = meta + slot * C::META_INTS;
                 m[0] = s; m[1] = h; m[2] = p; m[3] = nt; m[4] = ctx; m[5] = np;
+                m[6] = t0; m[7] = pre ? 1 : 0;
                 mbar_arrive_expect_tx(&desc_full[slot], D * 2);
                 bulk_copy_g2s(desc_q + slot * D, a.q + (static_cast<size_t>(s) * H + h) * D, D * 2,
                               &desc_full[slot]);
@@ -517,6 +685,9 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                     mbar_wait_drain(&desc_full[d % C::ND], (d / C::ND) & 1u);
             }
         }
+        // this grid must not complete before the shared-prefix kernel it
+        // reads from (a later kernel that waits for this one relies on it)
+        if (shared) grid_dependency_wait();
         return;
     }
 
@@ -524,6 +695,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     const int w = warp;
     float *probs = reinterpret_cast<float *>(smem + C::OFF_PROBS) + w * B;
     uint32_t kq = 0, dq = 0;
+    int ndefer = 0;   // this warp's deferred prefix merges
     while (true) {
         const int slot = static_cast<int>(dq % C::ND);
         bool w_ok = mbar_wait(&desc_full[slot], (dq / C::ND) & 1u, abort_flag, a.err);
@@ -531,7 +703,9 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         const int *m = meta + slot * C::META_INTS;
         const int s = m[0];
         if (s < 0) break;
-        const int h = m[1], p = m[2], nt = m[3], ctx = m[4], np = m[5];
+        const int h = m[1], p = m[2], nt = m[3], ctx = m[4], np = m[5], t0 = m[6];
+        // with a shared prefix, slot 0 of (s, h) holds the prefix kernel's partial
+        const int pre = m[7];
 
         float qf[8];
         const uint4 qraw =
@@ -554,7 +728,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                    mbar_wait(&full[st], (k / C::NS) & 1u, abort_flag, a.err);
             if (!__all_sync(kFull, w_ok)) return;
             if (stage_ok[st]) {
-                const int tok0 = (p * TPU + j) * B;
+                const int tok0 = (t0 + j) * B;
                 const int nvalid = min(B, ctx - tok0);
                 const uint8_t *ktile = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
                 consume_tile<E, D, B>(ktile, ktile + C::TILE_BYTES, qraw, qf, a.scale_log2, nvalid,
@@ -594,44 +768,46 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                 for (int e = 0; e < C::DPL; ++e) o[e] = fmaf(f, v[e], o[e]);
             }
             const size_t sh = static_cast<size_t>(s) * H + h;
-            if (np == 1) {
+            if (np == 1 && !pre) {
                 store_out<E, C::DPL>(a.out + sh * D + lane * C::DPL, o, L > 0.f ? 1.f / L : 0.f);
             } else {
-                const size_t pidx = sh * a.max_parts + p;
+                // a partial.  In shared-prefix mode slot 0 is the prefix
+                // kernel's alone (it may be writing it now, for any row of a
+                // group, even one this kernel decodes in full).
+                const int base = shared ? 1 : 0;
+                const size_t pidx = sh * a.max_parts + p + base;
                 if (lane == 0) reinterpret_cast<float2 *>(a.part_ml)[pidx] = make_float2(M, L);
                 store_f32<C::DPL>(a.part_acc + pidx * D + lane * C::DPL, o);
-                __threadfence();
-                __syncwarp();
-                uint32_t ticket = 0;
-                if (lane == 0) ticket = atomicAdd(&a.counters[2 + sh], 1u);
-                ticket = __shfl_sync(kFull, ticket, 0);
-                if (ticket == static_cast<uint32_t>(np - 1)) {
-                    // last partition of (s, h): combine all partials
+                bool last = true;
+                if (np > 1) {
                     __threadfence();
-                    const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml) + sh * a.max_parts;
-                    const float *pacc = a.part_acc + sh * a.max_parts * D + lane * C::DPL;
-                    float GM = -INFINITY;
-                    for (int i = lane; i < np; i += 32) GM = fmaxf(GM, __ldcg(pml + i).x);
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1)
-                        GM = fmaxf(GM, __shfl_xor_sync(kFull, GM, off));
-                    float GL = 0.f;
-                    float go[C::DPL];
-#pragma unroll
-                    for (int e = 0; e < C::DPL; ++e) go[e] = 0.f;
-#pragma unroll 4
-                    for (int i = 0; i < np; ++i) {
-                        const float2 ml = __ldcg(pml + i);
-                        float v[C::DPL];
-                        load_f32<C::DPL>(pacc + static_cast<size_t>(i) * D, v, true);
-                        const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - GM);
-                        GL = fmaf(f, ml.y, GL);
-#pragma unroll
-                        for (int e = 0; e < C::DPL; ++e) go[e] = fmaf(f, v[e], go[e]);
+                    __syncwarp();
+                    uint32_t ticket = 0;
+                    if (lane == 0) ticket = atomicAdd(&a.counters[2 + sh], 1u);
+                    ticket = __shfl_sync(kFull, ticket, 0);
+                    last = ticket == static_cast<uint32_t>(np - 1);
+                    if (last) {
+                        __threadfence();
+                        if (lane == 0) atomicExch(&a.counters[2 + sh], 0u);  // ready for the next call
                     }
-                    store_out<E, C::DPL>(a.out + sh * D + lane * C::DPL, go,
-                                          GL > 0.f ? 1.f / GL : 0.f);
-                    if (lane == 0) atomicExch(&a.counters[2 + sh], 0u);  // ready for the next call
+                }
+                if (last) {
+                    // the last partition of (s, h) combines all partials.  The
+                    // prefix partial comes from the previous launch: that
+                    // combine waits until this warp has no unit left, when the
+                    // prefix kernel has long finished.
+                    const int end = np + base;
+                    if (!pre) {
+                        combine_partials<E, D, C::DPL>(a, sh, base, end, lane);
+                    } else if (ndefer < C::DEFER) {
+                        if (lane == 0)
+                            defer[w * C::DEFER + ndefer] =
+                                make_uint2(static_cast<uint32_t>(sh), static_cast<uint32_t>(end));
+                        ++ndefer;
+                    } else {
+                        grid_dependency_wait();
+                        combine_partials<E, D, C::DPL>(a, sh, 0, end, lane);
+                    }
                 }
             }
             __syncwarp();
@@ -639,13 +815,21 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         if (lane == 0) mbar_arrive(&desc_empty[slot]);
         ++dq;
     }
+    if (ndefer > 0) {   // the deferred prefix merges
+        grid_dependency_wait();
+        __syncwarp();
+        for (int i = 0; i < ndefer; ++i) {
+            const uint2 e = defer[w * C::DEFER + i];
+            combine_partials<E, D, C::DPL>(a, e.x, 0, static_cast<int>(e.y), lane);
+        }
+    }
 }
 
 struct Variant {
     int dtype, head_dim, block_size;
     const void *kernel;
     int threads;
-    size_t (*smem_bytes)(int);
+    size_t (*smem_bytes)(int, int);
 };
 
 template <typename E, int D, int B>
@@ -710,6 +894,15 @@ cudaError_t prepare_decode_kernels(int device) {
     return cudaSuccess;
 }
 
+bool decode_fits(int dtype, int head_dim, int block_size, int num_seqs, int num_groups) {
+    const Variant *v = find_variant(dtype, head_dim, block_size);
+    int device = 0;
+    if (!v || cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+        return false;
+    return v->smem_bytes(num_seqs, num_groups) <=
+           static_cast<size_t>(g_max_dynamic_smem[device]);
+}
+
 cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int block_size,
                           int num_sms, cudaStream_t stream) {
     const Variant *v = find_variant(dtype, head_dim, block_size);
@@ -718,7 +911,8 @@ cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int b
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
     if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-    const size_t smem = v->smem_bytes(args.num_seqs);
+    const size_t smem =
+        v->smem_bytes(args.num_seqs, args.group_start != nullptr ? args.num_groups : -1);
     if (smem > static_cast<size_t>(g_max_dynamic_smem[device])) return cudaErrorInvalidConfiguration;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v->kernel, v->threads, smem);

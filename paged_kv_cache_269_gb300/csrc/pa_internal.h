@@ -28,6 +28,16 @@ struct DecodeArgs {
     float *part_acc;               // [S * H * max_parts * D]: unnormalised partial outputs
     uint32_t *counters;            // [2 + S * H]: work queue, finished CTAs, per-(s,h) tickets
     unsigned int *err;             // device error word
+    // Shared-prefix mode (group_start != nullptr): the prefix kernel, the
+    // previous launch on the stream, has written slot 0 of the partials of
+    // every row of each well-formed group with P_g > 0 (rows past rows_cap
+    // excepted).  This kernel covers the rest of each sequence that may use
+    // it and merges the two after waiting for the prefix kernel; the inputs
+    // were complete before that kernel let this one launch.
+    const int32_t *group_start;          // [num_groups + 1]
+    const int32_t *group_prefix_blocks;  // [num_groups]
+    int32_t num_groups;
+    int32_t rows_cap;                    // rows per group the prefix kernel computes
 };
 
 // Sizes of the two caller buffers of pa_decode_ws.
@@ -66,7 +76,20 @@ struct PrefillArgs {
     int32_t num_pairs;             // ceil(max_query_len / 256): pairs of 128-row tiles
     uint32_t *counters;            // [2]: next work item, CTAs done; zero on entry and exit
     unsigned int *err;
+    // Shared-prefix mode (group_prefix_blocks != nullptr).  The "sequences"
+    // are num_seqs groups of decode sequences: group g holds decode rows
+    // query_start[g] .. query_start[g + 1] - 1 (total_q = the decode batch),
+    // which share their first group_prefix_blocks[g] table entries.  Every
+    // row attends to all of those prefix keys (no causal mask), the table row
+    // read is the group's first sequence, and the result is written as a
+    // decode partial -- (max, sum) and the unnormalised output -- into slot 0
+    // of the row's partials.  block_tables is the decode batch's.
+    const int32_t *group_prefix_blocks;
+    float *part_ml;                // [S * H * max_parts * 2]
+    float *part_acc;               // [S * H * max_parts * D]
+    int32_t max_parts;
 };
+
 
 bool prefill_supported(int dtype, int head_dim, int block_size);
 cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k_cache,
@@ -86,6 +109,10 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int block_size,
                           int num_sms, cudaStream_t stream);
 bool decode_variant_supported(int dtype, int head_dim, int block_size);
+// Whether a decode launch of num_seqs sequences (and num_groups shared-prefix
+// groups; -1 for none) fits the current device's shared memory (after
+// prepare_decode_kernels).
+bool decode_fits(int dtype, int head_dim, int block_size, int num_seqs, int num_groups);
 cudaError_t prepare_decode_kernels(int device);
 
 cudaError_t launch_reshape_and_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,

@@ -341,6 +341,8 @@ __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu
 // One work item: a pair of query tiles of one (sequence, head).
 struct Item {
     int s, h, row0, q_first, q_len, ctx, ntiles, kmax, nkt;
+    int table_row;   // block-table row of the keys
+    bool causal;     // false: every row sees keys 0 .. ctx - 1 (shared-prefix mode)
 };
 
 // Work item w, heaviest pairs (latest positions) first: w = (level, s, h)
@@ -355,16 +357,37 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
     it.h = rem - it.s * a.num_heads;
     const int pair = a.num_pairs - 1 - level;
     it.q_first = __ldg(a.query_start + it.s);
-    it.q_len = __ldg(a.query_start + it.s + 1) - it.q_first;
-    it.ctx = __ldg(a.context_lens + it.s);
+    const int q_end = __ldg(a.query_start + it.s + 1);
+    // rows outside [0, total_q) (the difference taken without overflow)
+    const bool rows_bad = it.q_first < 0 || q_end < it.q_first || q_end > a.total_q;
+    it.q_len = rows_bad ? 0 : q_end - it.q_first;
     it.row0 = pair * kTiles * kBM;
+    if (a.group_prefix_blocks != nullptr) {
+        // shared-prefix mode: s is a group of decode rows, all of which see
+        // the whole prefix through the group's first row's table.  A
+        // malformed group is skipped here; the plan kernel reports it and
+        // leaves its rows to the decode kernel.
+        const int pb = __ldg(a.group_prefix_blocks + it.s);
+        if (rows_bad || it.q_len == 0 || it.row0 >= it.q_len || pb <= 0 ||
+            pb > a.max_blocks_per_seq)
+            return false;
+        it.ctx = pb * kB;
+        it.table_row = it.q_first;
+        it.causal = false;
+        it.ntiles = it.q_len - it.row0 > kBM ? 2 : 1;
+        it.kmax = it.ctx;
+        it.nkt = (it.kmax + kBN - 1) / kBN;
+        return true;
+    }
+    it.ctx = __ldg(a.context_lens + it.s);
+    it.table_row = it.s;
+    it.causal = true;
     // query rows past num_pairs * 256 (max_query_len understated) would never be
     // computed: reported once per sequence
     if (check && it.h == 0 && it.row0 == 0 && it.q_len > a.num_pairs * kTiles * kBM)
         atomicOr(a.err, PA_DEVERR_CONTEXT);
-    if (it.q_len <= 0 || it.row0 >= it.q_len) return false;
-    if (it.ctx > a.max_blocks_per_seq * kB || it.q_len > it.ctx || it.q_first < 0 ||
-        it.q_first + it.q_len > a.total_q) {
+    if (!rows_bad && (it.q_len == 0 || it.row0 >= it.q_len)) return false;
+    if (rows_bad || it.ctx > a.max_blocks_per_seq * kB || it.q_len > it.ctx) {
         if (check && it.h == 0 && it.row0 == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
         return false;
     }
@@ -378,6 +401,7 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
 // key tiles needed by query tile t of an item (0 if the tile is idle)
 __device__ __forceinline__ int tile_key_tiles(const Item &it, int t) {
     if (t >= it.ntiles) return 0;
+    if (!it.causal) return it.nkt;
     const int rows_t = min(kBM, it.q_len - it.row0 - t * kBM);
     return (it.ctx - it.q_len + it.row0 + t * kBM + rows_t + kBN - 1) / kBN;
 }
@@ -471,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++q_loads;
             const int nblk_needed = (it.kmax + kB - 1) / kB;
-            const int32_t *table = a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq;
+            const int32_t *table = a.block_tables + static_cast<size_t>(it.table_row) * a.max_blocks_per_seq;
             for (int j = 0; j < it.nkt && ok; ++j) {
                 const int st = gk % kStages;
                 const uint32_t ph = (gk / kStages) & 1;
@@ -694,9 +718,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             item_geometry(a, w, false, it);
             if (t >= it.ntiles) continue;
             const int rows_t = min(kBM, it.q_len - it.row0 - t * kBM);
-            const int first_pos = it.ctx - it.q_len + it.row0 + t * kBM;
-            const int my_nkt = (first_pos + rows_t + kBN - 1) / kBN;
-            const int pos = r < rows_t ? first_pos + r : -1;   // -1: padding row, all masked
+            // key position of the row (every row sits past the whole prefix
+            // in shared-prefix mode)
+            const int first_pos = it.causal ? it.ctx - it.q_len + it.row0 + t * kBM : it.ctx - 1;
+            const int my_nkt = tile_key_tiles(it, t);
+            const int pos = r < rows_t ? (it.causal ? first_pos + r : first_pos) : -1;   // -1: padding row, all masked
             const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < my_nkt && ok; ++j, ++n) {
@@ -824,7 +850,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[O_EMPTY + t]);
-            if (r < rows_t) {
+            if (r < rows_t && a.group_prefix_blocks != nullptr) {
+                // a decode partial for row s: the weights were 2^(x - (m - 6))
+                const size_t pidx =
+                    (static_cast<size_t>(it.q_first + it.row0 + t * kBM + r) * H + it.h) * a.max_parts;
+                reinterpret_cast<float2 *>(a.part_ml)[pidx] = make_float2(m_used - kBiasLog2, l);
+                float4 *dst = reinterpret_cast<float4 *>(a.part_acc + pidx * kD);
+#pragma unroll
+                for (int c4 = 0; c4 < kD / 4; ++c4)
+                    dst[c4] = make_float4(__uint_as_float(ov[4 * c4]), __uint_as_float(ov[4 * c4 + 1]),
+                                          __uint_as_float(ov[4 * c4 + 2]), __uint_as_float(ov[4 * c4 + 3]));
+            } else if (r < rows_t) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 uint16_t *dst =
                     a.out + (static_cast<size_t>(it.q_first + it.row0 + t * kBM + r) * H + it.h) * kD;

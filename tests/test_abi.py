@@ -141,6 +141,48 @@ def test_prefill_rejects(lib):
                           ctypes.byref(d), None) == -2
 
 
+def test_decode_shared_prefix_rejects(lib):
+    fake = ctypes.c_void_p(0x100000)           # never dereferenced: checks fail first
+    d = _dims()
+    ws_need = lib.pa_decode_shared_prefix_workspace_bytes(ctypes.byref(d), 8, 0)
+    ctr_need = lib.pa_decode_shared_prefix_counters_bytes(ctypes.byref(d))
+    # one extra partial slot per (sequence, head) for the prefix, always present
+    plain = lib.pa_decode_workspace_bytes(ctypes.byref(d), 8, 0)
+    assert ws_need > plain and ws_need >= d.num_seqs * d.num_heads * 2 * (d.head_dim + 2) * 4
+    assert ctr_need > lib.pa_decode_counters_bytes(ctypes.byref(d))
+
+    def call(dims=d, out=fake, gs=fake, gp=fake, G=1, maxg=4, scale=0.1, mb=8, ws=fake,
+             ws_n=ws_need, ctr=fake, ctr_n=ctr_need, pt=0):
+        return lib.pa_decode_shared_prefix_ws(
+            out, fake, fake, fake, fake, fake, scale, mb,
+            ctypes.byref(dims) if dims is not None else None, gs, gp, G, maxg, pt, ws, ws_n,
+            ctr, ctr_n, None)
+
+    assert call(dims=None) == -1
+    assert call(dims=_dims(D=64)) == -3          # the prefix kernel: head_dim 128 only
+    assert call(dims=_dims(B=32)) == -3          # and block_size 16
+    assert call(G=-1) == -2
+    assert call(maxg=-1) == -2
+    assert call(mb=0) == -2
+    assert call(pt=24) == -2                     # not a multiple of the block size
+    assert call(dims=_dims(S=0)) == 0            # nothing to do
+    assert call(out=None) == -1
+    assert call(gs=None) == -1
+    assert call(gp=None) == -1
+    assert call(out=ctypes.c_void_p(0x100002)) == -4
+    assert call(scale=float("nan")) == -2
+    assert call(ctr=None) == -5
+    assert call(ctr_n=ctr_need - 4) == -5
+    assert call(ctr=ctypes.c_void_p(0x100002)) == -5
+    assert call(ws=None) == -5                   # the prefix partials always need a workspace
+    assert call(ws_n=ws_need - 16) == -5
+    assert call(ws=ctypes.c_void_p(0x100008)) == -5
+    # more prefix work items (tile pairs x groups x heads) than an int32 counts
+    assert call(G=1 << 24, maxg=1 << 16) == -2
+    assert lib.pa_decode_shared_prefix(fake, fake, fake, fake, fake, fake, 0.1, 8,
+                                       ctypes.byref(_dims(D=64)), fake, fake, 1, 4, None) == -3
+
+
 def test_copy_blocks_rejects(lib):
     fake = ctypes.c_void_p(0x100000)
     d = _dims()

@@ -1,0 +1,210 @@
+"""GPU parity of the shared-prefix decode (pa_decode_shared_prefix_ws).
+
+The call must give pa_decode's output -- the fp64 oracle's, within the decode
+tolerance -- for every batch: groups of every size (one row, several 128-row
+tiles, several tile pairs), prefixes that end inside a 64-key tile, members
+whose suffix is empty or spans several partitions, sequences in no group, and
+every kind of misuse (a member whose table does not share the prefix, a
+context shorter than the prefix, an understated max_group_size, malformed
+group arrays), which must be decoded in full and flagged with DEVERR_PREFIX.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import assert_parity, to_numpy, torch_dtype, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_269_gb300 as pa
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    pa.lib()
+    pa.device_errors()  # start from a clear error word
+    return d
+
+
+def _buffers(dev, case, partition_tokens=0):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    l = pa.lib()
+    dims = pa.Dims(case.num_seqs, case.num_heads, case.head_dim, case.block_size,
+                   case.num_blocks, 1 if case.dtype == "bf16" else 0)
+    ws = l.pa_decode_shared_prefix_workspace_bytes(ctypes.byref(dims), case.max_blocks_per_seq,
+                                                   partition_tokens)
+    ctr = l.pa_decode_shared_prefix_counters_bytes(ctypes.byref(dims))
+    return (torch.zeros(ctr // 4, dtype=torch.int32, device=dev),
+            torch.empty(ws, dtype=torch.uint8, device=dev))
+
+
+def run_shared(case, gs, gp, dev, partition_tokens=0, max_group_size=None, counters=None,
+               workspace=None, tensors=None, allocate_in_library=False):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    d = tensors or upload(case, dev)
+    g_start = torch.from_numpy(np.ascontiguousarray(gs, dtype=np.int32)).to(dev)
+    g_pre = torch.from_numpy(np.ascontiguousarray(gp, dtype=np.int32)).to(dev)
+    out = torch.full(case.q.shape, float("nan"), dtype=torch_dtype(case), device=dev)
+    pa.decode_shared_prefix(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                            d["context_lens"], case.scale, g_start, g_pre,
+                            max_group_size=max_group_size, partition_tokens=partition_tokens,
+                            counters=counters, workspace=workspace,
+                            allocate_in_library=allocate_in_library)
+    flags = pa.device_errors()
+    return to_numpy(out, case), flags
+
+
+# a batch with every shape the two kernels must agree on
+def _layout(rng):
+    return [
+        (5, [80, 81, 700]),                              # prefix ends inside a key tile; empty suffix
+        (0, [33, 1000]),                                 # in no group
+        (8, [int(c) for c in rng.integers(128, 600, 130)]),   # 130 rows: two 128-row tiles
+        (1, [20]),                                       # a group of one
+        (40, [int(c) for c in rng.integers(641, 1400, 300)]),  # two tile pairs; long suffixes
+        (3, [48, 49, 63, 64, 65]),                       # suffixes of 0, 1, 15, 16, 17 tokens
+    ]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("partition_tokens", [0, 256])
+def test_ragged_groups(dev, dtype, partition_tokens):
+    rng = np.random.default_rng(21)
+    case, gs, gp = workloads.build_grouped_case("groups", _layout(rng), num_heads=2,
+                                                head_dim=128, seed=21, dtype=dtype)
+    ctr, ws = _buffers(dev, case, partition_tokens)
+    got, flags = run_shared(case, gs, gp, dev, partition_tokens, counters=ctr, workspace=ws)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), f"groups {dtype} P={partition_tokens}",
+                  dtype=dtype)
+    assert int(ctr.count_nonzero()) == 0        # the counters are left zeroed
+
+
+def test_shared_prefix_workload_full_size(dev):
+    """The 128-sequence, 512-token-prompt batch, in the launch configuration the
+    benchmark times: one group of 128 sharing 32 blocks."""
+    case = workloads.make_workload("shared_prefix")
+    gs = np.array([0, case.num_seqs], dtype=np.int32)
+    gp = np.array([case.shared_prefix_blocks], dtype=np.int32)
+    got, flags = run_shared(case, gs, gp, dev)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), "shared_prefix (shared reads)")
+
+
+def test_matches_plain_decode_and_library_allocation(dev):
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    rng = np.random.default_rng(5)
+    case, gs, gp = workloads.build_grouped_case("alloc", _layout(rng)[:4], num_heads=4,
+                                                head_dim=128, seed=5)
+    d = upload(case, dev)
+    got, flags = run_shared(case, gs, gp, dev, tensors=d, allocate_in_library=True)
+    assert flags == 0
+    ref = oracle.decode_case(case)
+    assert_parity(got, ref, "library-allocated buffers")
+    plain = torch.empty(case.q.shape, dtype=torch.float16, device=dev)
+    pa.decode(plain, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+              case.scale)
+    assert_parity(plain.cpu().numpy(), ref, "plain decode")
+    # two correct answers: they differ by rounding only
+    diff = np.abs(got.astype(np.float64) - plain.cpu().numpy().astype(np.float64))
+    assert float(diff.max()) <= 2e-3
+
+
+def test_with_new_tokens_after_reshape(dev):
+    """reshape_and_cache, then the two shared-prefix launches, back to back on one
+    stream: each sequence's new token (in its private suffix) must be seen."""
+    import paged_kv_cache_269_gb300 as pa
+    rng = np.random.default_rng(9)
+    layout = [(4, [int(c) for c in rng.integers(70, 400, 40)]), (0, [17, 300]),
+              (12, [int(c) for c in rng.integers(200, 900, 20)])]
+    case, gs, gp = workloads.build_grouped_case("step", layout, num_heads=4, head_dim=128,
+                                                seed=9, new_tokens=True)
+    d = upload(case, dev)
+    pa.reshape_and_cache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    got, flags = run_shared(case, gs, gp, dev, tensors=d)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), "after reshape_and_cache")
+
+
+def test_counters_serve_calls_of_any_size(dev):
+    """One zeroed counter buffer and workspace, sized for the largest batch,
+    serve a sequence of calls of different sizes (each leaves them zeroed)."""
+    rng = np.random.default_rng(13)
+    big, gs_b, gp_b = workloads.build_grouped_case("big", _layout(rng), num_heads=2,
+                                                   head_dim=128, seed=13)
+    small, gs_s, gp_s = workloads.build_grouped_case("small", [(2, [40, 50]), (0, [7])],
+                                                     num_heads=2, head_dim=128, seed=14,
+                                                     max_blocks_per_seq=big.max_blocks_per_seq)
+    ctr, ws = _buffers(dev, big, 256)
+    for case, gs, gp in ((big, gs_b, gp_b), (small, gs_s, gp_s), (big, gs_b, gp_b)):
+        got, flags = run_shared(case, gs, gp, dev, 256, counters=ctr, workspace=ws)
+        assert flags == 0
+        assert_parity(got, oracle.decode_case(case), case.name)
+        assert int(ctr.count_nonzero()) == 0
+
+
+# ----------------------------------------------------------------------------
+# misuse: always pa_decode's output, plus the DEVERR_PREFIX flag
+# ----------------------------------------------------------------------------
+
+def _misuse_case():
+    rng = np.random.default_rng(17)
+    return workloads.build_grouped_case(
+        "misuse", [(6, [int(c) for c in rng.integers(100, 500, 12)]), (0, [60]),
+                   (3, [int(c) for c in rng.integers(50, 300, 300)])],
+        num_heads=2, head_dim=128, seed=17)
+
+
+def _expect_full_decode(dev, case, gs, gp, what, **kw):
+    import paged_kv_cache_269_gb300 as pa
+    ctr, ws = _buffers(dev, case)
+    got, flags = run_shared(case, gs, gp, dev, counters=ctr, workspace=ws, **kw)
+    assert flags & pa.DEVERR_PREFIX, what
+    assert (flags & ~pa.DEVERR_PREFIX) == 0, what
+    assert_parity(got, oracle.decode_case(case), what)
+    assert int(ctr.count_nonzero()) == 0, what
+
+
+def test_member_with_a_different_prefix_block(dev):
+    case, gs, gp = _misuse_case()
+    # member 3 of the first group points its block 2 at another block of the pool
+    spare = int(case.block_tables[20, 0])
+    case.block_tables[3, 2] = spare
+    workloads.poison_unused(case)
+    _expect_full_decode(dev, case, gs, gp, "foreign prefix block")
+
+
+def test_member_shorter_than_the_prefix(dev):
+    case, gs, gp = _misuse_case()
+    case.context_lens[5] = 6 * case.block_size - 3       # inside the group's prefix
+    workloads.poison_unused(case)
+    _expect_full_decode(dev, case, gs, gp, "context shorter than the prefix")
+
+
+def test_understated_max_group_size(dev):
+    case, gs, gp = _misuse_case()
+    # the 300-row group needs two tile pairs; one is planned: rows 256.. decode in full
+    _expect_full_decode(dev, case, gs, gp, "max_group_size understated", max_group_size=100)
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "past_batch", "prefix_too_long"])
+def test_malformed_group_arrays(dev, bad):
+    case, gs, gp = _misuse_case()
+    gs, gp = gs.copy(), gp.copy()
+    if bad == "decreasing":
+        gs[1], gs[2] = gs[2], gs[1]
+    elif bad == "past_batch":
+        gs[-1] = case.num_seqs + 5
+    else:
+        gp[0] = case.max_blocks_per_seq + 1
+    _expect_full_decode(dev, case, gs, gp, bad, max_group_size=int(np.abs(np.diff(gs)).max()))

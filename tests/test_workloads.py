@@ -86,3 +86,27 @@ def test_out_of_blocks():
     rng = np.random.default_rng(0)
     with pytest.raises(workloads.OutOfBlocks):
         workloads.allocate_tables(np.array([40, 40]), 16, 5, 4, rng)
+
+
+def test_grouped_case_tables():
+    layout = [(5, [80, 81, 700]), (0, [33, 1000]), (2, [20, 40]), (1, [16])]
+    case, gs, gp = workloads.build_grouped_case("g", layout, num_heads=2, head_dim=64, seed=3)
+    assert gs.tolist() == [0, 3, 5, 7, 8] and gp.tolist() == [5, 0, 2, 1]
+    nb = case.blocks_used()
+    private, prefixes = [], []
+    for g, (P, _) in enumerate(layout):
+        rows = case.block_tables[gs[g]:gs[g + 1]]
+        if P:
+            assert (rows[:, :P] == rows[0, :P]).all()      # every member starts with the prefix
+            prefixes.extend(rows[0, :P].tolist())
+        for i, s in enumerate(range(gs[g], gs[g + 1])):
+            row = case.block_tables[s]
+            assert (row[:nb[s]] >= 0).all() and (row[:nb[s]] < case.num_blocks).all()
+            assert (row[nb[s]:] == -1).all()
+            private.extend(row[P:nb[s]].tolist())
+    # every block is either one group's prefix or one sequence's own
+    assert len(private + prefixes) == len(set(private + prefixes))
+    # blocks no table references hold NaN; referenced ones hold values
+    spare = sorted(set(range(case.num_blocks)) - set(private + prefixes))
+    assert spare and np.isnan(case.k_cache[spare].astype(np.float32)).all()
+    assert np.isfinite(case.k_cache[prefixes].astype(np.float32)).all()

@@ -215,13 +215,15 @@ def build_case(name: str, context_lens, *, num_heads: int, head_dim: int,
                num_blocks: Optional[int] = None, spare_frac: float = 0.10,
                max_blocks_per_seq: Optional[int] = None,
                shared_prefix_blocks: int = 0, new_tokens: bool = False,
-               poison: bool = True, values: bool = True, dtype: str = "f16") -> DecodeCase:
+               poison: bool = True, values: bool = True, dtype: str = "f16",
+               tables: Optional[np.ndarray] = None) -> DecodeCase:
     """Generic builder; the named workloads below are thin wrappers.
 
     The pool holds exactly the blocks the tables use plus `spare_frac` spare
     blocks (left NaN), unless num_blocks is given.  values=False skips drawing
     q/K/V (the arrays are allocated but left unfilled) for callers that only
-    need lengths and tables.
+    need lengths and tables.  `tables` (with num_blocks and
+    max_blocks_per_seq) supplies ready-made block tables instead.
     """
     rng = np.random.default_rng(seed)
     ctx = np.asarray(context_lens, dtype=np.int32)
@@ -233,10 +235,15 @@ def build_case(name: str, context_lens, *, num_heads: int, head_dim: int,
         needed = shared_prefix_blocks + sum(max(0, n - shared_prefix_blocks) for n in nb)
     else:
         needed = sum(nb)
-    if num_blocks is None:
-        num_blocks = max(1, needed + int(math.ceil(spare_frac * needed)))
-    tables = allocate_tables(ctx, block_size, num_blocks, max_blocks_per_seq, rng,
-                             shared_prefix_blocks)
+    if tables is not None:
+        if num_blocks is None or tables.shape != (S, max_blocks_per_seq):
+            raise ValueError("ready-made tables need num_blocks and a matching max_blocks_per_seq")
+        tables = np.ascontiguousarray(tables, dtype=np.int32)
+    else:
+        if num_blocks is None:
+            num_blocks = max(1, needed + int(math.ceil(spare_frac * needed)))
+        tables = allocate_tables(ctx, block_size, num_blocks, max_blocks_per_seq, rng,
+                                 shared_prefix_blocks)
     H, D = num_heads, head_dim
     st = STORAGE[dtype]
     q = np.empty((S, H, D), dtype=st)
@@ -257,6 +264,57 @@ def build_case(name: str, context_lens, *, num_heads: int, head_dim: int,
     if new_tokens:
         add_new_tokens(case)
     return case
+
+
+def build_grouped_case(name: str, layout, *, num_heads: int, head_dim: int, seed: int,
+                       block_size: int = BLOCK_SIZE, spare_frac: float = 0.10,
+                       max_blocks_per_seq: Optional[int] = None, dtype: str = "f16",
+                       new_tokens: bool = False):
+    """A decode batch in groups that share a prompt prefix.
+
+    layout = [(P, [ctx, ...]), ...] lists consecutive groups of sequences.  In
+    a group with P > 0 the first P blocks are popped once from the shuffled
+    free list and start every member's table (a shared system prompt, or
+    samples forked from one prompt: "vLLM 2026 推理引擎全解", §2.3); each
+    member then pops its private blocks.  Sequences of a P = 0 entry share
+    nothing.  Unused slots are NaN-poisoned.  Returns (case, group_start
+    [G + 1] int32, group_prefix_blocks [G] int32), one group per entry.
+    """
+    rng = np.random.default_rng(np.random.SeedSequence(seed, spawn_key=(1,)))
+    lens = [int(c) for _, members in layout for c in members]
+    nb = [blocks_needed(c, block_size) for c in lens]
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max(1, max(nb) if nb else 1)
+    needed = 0
+    i = 0
+    for P, members in layout:
+        if P:
+            needed += P
+        for _ in members:
+            needed += max(0, nb[i] - P)
+            i += 1
+    num_blocks = max(1, needed + int(math.ceil(spare_frac * needed)))
+    free = deque(int(b) for b in rng.permutation(num_blocks))
+    tables = np.full((len(lens), max_blocks_per_seq), -1, dtype=np.int32)
+    group_start, group_prefix = [0], []
+    s = 0
+    for P, members in layout:
+        prefix = [free.popleft() for _ in range(P)]
+        for _ in members:
+            if nb[s] > max_blocks_per_seq:
+                raise ValueError(f"sequence {s} needs {nb[s]} blocks > max_blocks_per_seq")
+            row = prefix[:min(nb[s], P)]
+            row += [free.popleft() for _ in range(nb[s] - len(row))]
+            tables[s, :nb[s]] = row
+            s += 1
+        group_start.append(s)
+        group_prefix.append(P)
+    case = build_case(name, lens, num_heads=num_heads, head_dim=head_dim, seed=seed,
+                      block_size=block_size, num_blocks=num_blocks,
+                      max_blocks_per_seq=max_blocks_per_seq, dtype=dtype, tables=tables,
+                      new_tokens=new_tokens)
+    return (case, np.asarray(group_start, dtype=np.int32),
+            np.asarray(group_prefix, dtype=np.int32))
 
 
 def build_prefill_case(name: str, context_lens, query_lens, *, num_heads: int, head_dim: int,

@@ -113,7 +113,7 @@ struct Cfg {
     __host__ __device__ static size_t seq_ints(int num_seqs, int num_groups) {
         const size_t S = static_cast<size_t>(num_seqs);
         return num_groups < 0 ? 2 * S + 1
-                              : 4 * S + 1 + static_cast<size_t>(num_groups) + 1 + KEYS;
+                              : 4 * S + 1 + 2 * static_cast<size_t>(num_groups) + 1 + KEYS;
     }
     static size_t smem_bytes(int num_seqs, int num_groups) {
         size_t n = static_cast<size_t>(OFF_SEQ) + seq_ints(num_seqs, num_groups) * 4;
@@ -415,7 +415,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     int *start_of = ctx_of + S;                                // [S]
     int *order = start_of + S;                                 // [S] work order: position -> s
     int *gstart = order + S;                                   // [G + 1]
-    int *classes = gstart + G + 1;                             // [KEYS]
+    int *gpre = gstart + G + 1;                                // [G]
+    int *classes = gpre + G;                                   // [KEYS]
     uint2 *defer = reinterpret_cast<uint2 *>(
         smem + (C::OFF_SEQ + C::seq_ints(S, G) * 4 + 7) / 8 * 8);   // [NC][DEFER]
 
@@ -448,23 +449,25 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     const int ctx_cap = a.max_blocks_per_seq * B;
     bool malformed = false;
     if (shared) {
-        // the group arrays: non-decreasing within [0, S], P_g within the table
-        for (int g = threadIdx.x; g <= G; g += blockDim.x) gstart[g] = __ldg(a.group_start + g);
+        // one round of global loads: the group arrays and the lengths
+        for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+            gstart[g] = __ldg(a.group_start + g);
+            if (g < G) gpre[g] = __ldg(a.group_prefix_blocks + g);
+        }
+        for (int s = threadIdx.x; s < S; s += blockDim.x) ctx_of[s] = a.context_lens[s];
         __syncthreads();
+        // the group arrays: non-decreasing within [0, S], P_g within the table
         bool bad = false;
         for (int g = threadIdx.x; g <= G; g += blockDim.x) {
             const int lo = gstart[g];
             bad = bad || lo < 0 || lo > S;
-            if (g < G) {
-                const int pb = __ldg(a.group_prefix_blocks + g);
-                bad = bad || gstart[g + 1] < lo || pb < 0 || pb > a.max_blocks_per_seq;
-            }
+            if (g < G) bad = bad || gstart[g + 1] < lo || gpre[g] < 0 || gpre[g] > a.max_blocks_per_seq;
         }
         malformed = __syncthreads_or(bad) != 0;
         if (malformed && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_PREFIX);
     }
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
-        const int c_in = a.context_lens[s];
+        const int c_in = shared ? ctx_of[s] : a.context_lens[s];
         int c = c_in;
         if (c < 0 || c > ctx_cap) {
             atomicOr(a.err, PA_DEVERR_CONTEXT);
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                     const int mid = (lo + hi + 1) >> 1;
                     if (gstart[mid] <= s) lo = mid; else hi = mid - 1;
                 }
-                const int pb = __ldg(a.group_prefix_blocks + lo);
+                const int pb = gpre[lo];
                 if (s < gstart[lo + 1] && pb > 0) {
                     // rows the prefix kernel covers, whose context holds the prefix
                     if (c_in >= pb * B && c_in <= ctx_cap && s - gstart[lo] < a.rows_cap) {

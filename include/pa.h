@@ -456,6 +456,22 @@ int pa_kvm_slot(const pa_kv_manager *m, int32_t seq, int32_t token, int32_t *slo
 int pa_kvm_block_tables(const pa_kv_manager *m, const int32_t *seqs, int32_t num_seqs,
                         int32_t *tables_out, int32_t row_len, int32_t *context_lens_out);
 
+/* Groups for pa_decode_shared_prefix from the manager's sharing records, for
+ * the batch rows seqs[0 .. num_seqs) in that order (negative ids are padding
+ * rows).  Consecutive rows form a group when their tables start with the same
+ * physical blocks: the group's prefix is what its first two rows share, and
+ * every later member shares at least that much with the first row.  Only
+ * blocks that are full in every member count (a block still being filled,
+ * shared after a fork, is left to each member's suffix).  Rows that share
+ * nothing with the next row are gathered into groups of prefix 0.  Every row
+ * belongs to exactly one group.  Writes group_start_out[num_groups + 1] and
+ * group_prefix_out[num_groups] (host arrays of max_groups + 1 and max_groups
+ * entries); PA_ERR_SHAPE if more than max_groups groups are needed or an id
+ * is unknown.  Sharers must be adjacent in the batch to be grouped. */
+int pa_kvm_prefix_groups(const pa_kv_manager *m, const int32_t *seqs, int32_t num_seqs,
+                         int32_t *group_start_out, int32_t *group_prefix_out, int32_t max_groups,
+                         int32_t *num_groups_out);
+
 /*
  * Wait for `stream`, then return (in *flags, host) and clear the current
  * device's error word: an OR of PA_DEVERR_* bits set by kernels since the last

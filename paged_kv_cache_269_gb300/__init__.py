@@ -25,7 +25,8 @@ from . import build as _build
 
 __all__ = ["PaError", "Dims", "KVManager", "lib", "reshape_and_cache", "copy_blocks", "decode",
            "decode_shared_prefix", "selftest_wait_timeout",
-           "prefill", "decode_workspace_bytes",
+           "prefill", "decode_workspace_bytes", "decode_shared_prefix_workspace_bytes",
+           "decode_shared_prefix_counters_bytes",
            "decode_counters_bytes", "device_errors", "reset_workspaces", "version", "DEVERR_TABLE", "DEVERR_CONTEXT",
            "DEVERR_SLOT", "DEVERR_TIMEOUT", "DEVERR_PREFIX"]
 
@@ -48,7 +49,8 @@ EXPORTS = ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", 
            "pa_kvm_add_sequence", "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free",
            "pa_kvm_context_len", "pa_kvm_slot", "pa_kvm_block_tables", "pa_selftest_wait_timeout",
            "pa_decode_shared_prefix", "pa_decode_shared_prefix_ws",
-           "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix_counters_bytes")
+           "pa_decode_shared_prefix_workspace_bytes", "pa_decode_shared_prefix_counters_bytes",
+           "pa_kvm_prefix_groups")
 _SIZE_ERROR = (1 << 64) - 1
 
 
@@ -118,9 +120,10 @@ def _declare(l):
     l.pa_kvm_context_len.argtypes = [vp, i32]
     l.pa_kvm_slot.argtypes = [vp, i32, i32, i32p]
     l.pa_kvm_block_tables.argtypes = [vp, vp, i32, vp, i32, vp]
+    l.pa_kvm_prefix_groups.argtypes = [vp, vp, i32, vp, vp, i32, ctypes.POINTER(ctypes.c_int32)]
     for name in ("pa_kvm_num_free_blocks", "pa_kvm_refcount", "pa_kvm_add_sequence",
                  "pa_kvm_fork", "pa_kvm_append", "pa_kvm_free", "pa_kvm_context_len",
-                 "pa_kvm_slot", "pa_kvm_block_tables"):
+                 "pa_kvm_slot", "pa_kvm_block_tables", "pa_kvm_prefix_groups"):
         getattr(l, name).restype = i32
     for name in ("pa_reshape_and_cache", "pa_copy_blocks", "pa_decode", "pa_prefill", "pa_prefill_ws",
                  "pa_decode_ws", "pa_decode_shared_prefix", "pa_decode_shared_prefix_ws",
@@ -346,6 +349,28 @@ def decode_counters_bytes(num_seqs, num_heads, head_dim=128, block_size=16, num_
     n = lib().pa_decode_counters_bytes(ctypes.byref(dims))
     if n == 0:
         raise PaError(-2, "pa_decode_counters_bytes: invalid sizes")
+    return n
+
+
+def decode_shared_prefix_workspace_bytes(num_seqs, num_heads, head_dim, block_size, num_blocks,
+                                         max_blocks_per_seq, partition_tokens=0,
+                                         dtype=DTYPE_F16) -> int:
+    """Bytes of workspace pa_decode_shared_prefix_ws needs."""
+    dims = Dims(num_seqs, num_heads, head_dim, block_size, num_blocks, dtype)
+    n = lib().pa_decode_shared_prefix_workspace_bytes(ctypes.byref(dims), max_blocks_per_seq,
+                                                      partition_tokens)
+    if n == _SIZE_ERROR:
+        raise PaError(-2, "pa_decode_shared_prefix_workspace_bytes: invalid sizes")
+    return n
+
+
+def decode_shared_prefix_counters_bytes(num_seqs, num_heads, head_dim=128, block_size=16,
+                                        num_blocks=1) -> int:
+    """Bytes of the (zeroed, reusable) counter buffer pa_decode_shared_prefix_ws needs."""
+    dims = Dims(num_seqs, num_heads, head_dim, block_size, num_blocks)
+    n = lib().pa_decode_shared_prefix_counters_bytes(ctypes.byref(dims))
+    if n == 0:
+        raise PaError(-2, "pa_decode_shared_prefix_counters_bytes: invalid sizes")
     return n
 
 
@@ -582,6 +607,21 @@ class KVManager:
                                            tables.ctypes.data, row_len, lens.ctypes.data),
                "pa_kvm_block_tables")
         return tables, lens
+
+    def prefix_groups(self, seqs, max_groups=None):
+        """(group_start [G + 1] int32, group_prefix_blocks [G] int32) for the
+        batch rows `seqs`, as decode_shared_prefix takes them: runs of adjacent
+        rows whose tables start with the same full blocks (pa_kvm_prefix_groups)."""
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, dtype=np.int32)
+        cap = len(ids) if max_groups is None else int(max_groups)
+        starts = np.empty(cap + 1, np.int32)
+        pre = np.empty(max(cap, 1), np.int32)
+        g = ctypes.c_int32(0)
+        _check(self._l.pa_kvm_prefix_groups(self._h, ids.ctypes.data, len(ids), starts.ctypes.data,
+                                            pre.ctypes.data, cap, ctypes.byref(g)),
+               "pa_kvm_prefix_groups")
+        return starts[:g.value + 1].copy(), pre[:g.value].copy()
 
 
 def selftest_wait_timeout(stream=None, device=None):

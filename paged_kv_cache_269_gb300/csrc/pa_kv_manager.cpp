@@ -235,4 +235,62 @@ int pa_kvm_block_tables(const pa_kv_manager *m, const int32_t *seqs, int32_t num
     return PA_OK;
 }
 
+int pa_kvm_prefix_groups(const pa_kv_manager *m, const int32_t *seqs, int32_t num_seqs,
+                         int32_t *group_start_out, int32_t *group_prefix_out, int32_t max_groups,
+                         int32_t *num_groups_out) {
+    if (!m || !num_groups_out || (num_seqs > 0 && (!seqs || !group_start_out || !group_prefix_out)))
+        return PA_ERR_NULL;
+    if (num_seqs < 0 || max_groups < 0) return PA_ERR_SHAPE;
+    for (int32_t i = 0; i < num_seqs; ++i)
+        if (seqs[i] >= 0 && !m->valid_seq(seqs[i])) return PA_ERR_SHAPE;
+    // leading blocks of row i that are full (a padding row has none)
+    auto full = [&](int32_t i) -> int32_t {
+        return seqs[i] < 0 ? 0 : m->seqs[seqs[i]].len / m->block_size;
+    };
+    // leading full blocks rows i and j have in common
+    auto common = [&](int32_t i, int32_t j) -> int32_t {
+        const int32_t n = full(i) < full(j) ? full(i) : full(j);
+        if (n == 0) return 0;   // also every padding row
+        const std::vector<int32_t> &a = m->seqs[seqs[i]].blocks, &b = m->seqs[seqs[j]].blocks;
+        int32_t c = 0;
+        while (c < n && a[c] == b[c]) ++c;
+        return c;
+    };
+    int32_t g = 0;
+    bool open_unshared = false;  // the last group holds rows that share nothing
+    auto emit = [&](int32_t start, int32_t prefix) -> bool {
+        if (g >= max_groups) return false;
+        group_start_out[g] = start;
+        group_prefix_out[g] = prefix;
+        ++g;
+        return true;
+    };
+    int32_t i = 0;
+    while (i < num_seqs) {
+        // the group's prefix is what row i shares with row i + 1; the run goes
+        // on while later rows share at least that much with row i
+        const int32_t P = i + 1 < num_seqs ? common(i, i + 1) : 0;
+        int32_t j = i + 1;
+        if (P > 0)
+            while (j < num_seqs && common(i, j) >= P) ++j;
+        if (P > 0) {
+            if (!emit(i, P)) return PA_ERR_SHAPE;
+            open_unshared = false;
+            i = j;
+        } else {
+            if (!open_unshared && !emit(i, 0)) return PA_ERR_SHAPE;
+            open_unshared = true;
+            ++i;
+        }
+    }
+    if (num_seqs > 0) {
+        if (max_groups < g || !group_start_out) return PA_ERR_SHAPE;
+        group_start_out[g] = num_seqs;
+    } else if (group_start_out) {
+        group_start_out[0] = 0;
+    }
+    *num_groups_out = g;
+    return PA_OK;
+}
+
 }  // extern "C"

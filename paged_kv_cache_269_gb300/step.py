@@ -12,6 +12,11 @@ be captured once as a CUDA graph and replayed every step.  Copy-on-write
 copies reported by the manager are made eagerly, before the step, with
 copy_blocks.
 
+With max_groups > 0 the step decodes with decode_shared_prefix: the caller
+also hands over the groups of adjacent rows that share prompt blocks (e.g.
+KVManager.prefix_groups of the batch), staged with the other inputs; unused
+group slots are empty, so the shapes still never change.
+
 This module only orchestrates calls into libpa; all arithmetic runs in its
 kernels.
 """
@@ -19,12 +24,14 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import copy_blocks, decode, decode_counters_bytes, decode_workspace_bytes, reshape_and_cache
+from . import (copy_blocks, decode, decode_counters_bytes, decode_shared_prefix,
+               decode_shared_prefix_counters_bytes, decode_shared_prefix_workspace_bytes,
+               decode_workspace_bytes, reshape_and_cache)
 
 
 class DecodeStep:
     def __init__(self, k_cache, v_cache, max_seqs, max_blocks_per_seq, scale, use_graph=True,
-                 partition_tokens=0, stream=None, host_out=False):
+                 partition_tokens=0, stream=None, host_out=False, max_groups=0):
         import torch
         self.torch = torch
         self.k_cache, self.v_cache = k_cache, v_cache
@@ -36,6 +43,7 @@ class DecodeStep:
         self.stream = stream or torch.cuda.Stream(self.dev)
         self.use_graph = use_graph
         self.graph = None
+        self.G = int(max_groups)
         S, MB = max_seqs, max_blocks_per_seq
         # packed layout: name -> (offset, shape, numpy dtype, torch dtype), 256-byte aligned
         el = np.float16 if self.dtype == torch.float16 else np.uint16
@@ -43,6 +51,9 @@ class DecodeStep:
                   ("v_new", (S, H, D), el, self.dtype), ("slots", (S,), np.int32, torch.int32),
                   ("tables", (S, MB), np.int32, torch.int32),
                   ("lens", (S,), np.int32, torch.int32)]
+        if self.G > 0:
+            fields += [("gstart", (self.G + 1,), np.int32, torch.int32),
+                       ("gpre", (self.G,), np.int32, torch.int32)]
         self.layout, off = {}, 0
         for name, shape, nd, td in fields:
             nbytes = int(np.prod(shape)) * np.dtype(nd).itemsize
@@ -60,19 +71,28 @@ class DecodeStep:
         # memory (part of the graph), read it after the stream reaches it
         self.out_host = (torch.empty((S, H, D), dtype=self.dtype).pin_memory()
                          if host_out else None)
-        ws = decode_workspace_bytes(S, H, D, B, N, MB, partition_tokens,
-                                    dtype=1 if self.dtype == torch.bfloat16 else 0)
+        dt = 1 if self.dtype == torch.bfloat16 else 0
+        if self.G > 0:
+            ws = decode_shared_prefix_workspace_bytes(S, H, D, B, N, MB, partition_tokens, dtype=dt)
+            ctr = decode_shared_prefix_counters_bytes(S, H, D, B, N)
+        else:
+            ws = decode_workspace_bytes(S, H, D, B, N, MB, partition_tokens, dtype=dt)
+            ctr = decode_counters_bytes(S, H, D, B, N)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
-        self.counters = torch.zeros(decode_counters_bytes(S, H, D, B, N) // 4, dtype=torch.int32,
-                                    device=self.dev)
+        self.counters = torch.zeros(ctr // 4, dtype=torch.int32, device=self.dev)
         self.h["slots"][:] = -1
         self.h["lens"][:] = 0
         self.h["tables"][:] = -1
+        if self.G > 0:
+            self.h["gstart"][:] = 0
+            self.h["gpre"][:] = 0
 
-    def prepare(self, q, k_new, v_new, slots, tables, lens):
+    def prepare(self, q, k_new, v_new, slots, tables, lens, groups=None):
         """Stage one step's inputs (numpy; n <= max_seqs rows) into the pinned
-        buffer; rows n .. max_seqs-1 become padding.  Waits for the previous
-        step first, whose copy reads the same pinned buffer."""
+        buffer; rows n .. max_seqs-1 become padding.  groups (with
+        max_groups > 0): (group_start [G + 1], group_prefix_blocks [G]) over
+        the n rows, G <= max_groups; None shares nothing.  Waits for the
+        previous step first, whose copy reads the same pinned buffer."""
         self.stream.synchronize()
         n = len(lens)
         if n > self.S:
@@ -86,14 +106,31 @@ class DecodeStep:
         h["tables"][n:] = -1
         h["lens"][:n] = lens
         h["lens"][n:] = 0
+        if self.G > 0:
+            gs, gp = groups if groups is not None else (np.zeros(1, np.int32), np.zeros(0, np.int32))
+            g = len(gp)
+            if g > self.G or len(gs) != g + 1:
+                raise ValueError("more groups than max_groups, or inconsistent group arrays")
+            h["gstart"][:g + 1] = gs
+            h["gstart"][g + 1:] = gs[-1]
+            h["gpre"][:g] = gp
+            h["gpre"][g:] = 0
+        elif groups is not None:
+            raise ValueError("groups need a step built with max_groups > 0")
 
     def _body(self):
         d = self.d
         self.devbuf.copy_(self.host, non_blocking=True)
         reshape_and_cache(d["k_new"], d["v_new"], self.k_cache, self.v_cache, d["slots"])
-        decode(self.out, d["q"], self.k_cache, self.v_cache, d["tables"], d["lens"], self.scale,
-               partition_tokens=self.partition_tokens, workspace=self.workspace,
-               counters=self.counters)
+        if self.G > 0:
+            decode_shared_prefix(self.out, d["q"], self.k_cache, self.v_cache, d["tables"],
+                                 d["lens"], self.scale, d["gstart"], d["gpre"],
+                                 max_group_size=self.S, partition_tokens=self.partition_tokens,
+                                 workspace=self.workspace, counters=self.counters)
+        else:
+            decode(self.out, d["q"], self.k_cache, self.v_cache, d["tables"], d["lens"],
+                   self.scale, partition_tokens=self.partition_tokens, workspace=self.workspace,
+                   counters=self.counters)
         if self.out_host is not None:
             self.out_host.copy_(self.out, non_blocking=True)
 

@@ -5,7 +5,9 @@ parent as parallel samples), grow by one token per step, and finish; the
 manager hands out slots and copy-on-write copies, the step writes the new K/V
 and decodes.  After every step the output is compared with the oracle run on a
 host mirror of the cache that receives the same copies and writes.  The loop
-runs eagerly and replayed from a CUDA graph."""
+runs eagerly and replayed from a CUDA graph, with plain decode and with the
+shared-prefix decode (the batch ordered so that sharers are adjacent, the
+groups taken from the manager's sharing records every step)."""
 import numpy as np
 import pytest
 
@@ -35,8 +37,10 @@ def _normal(rng, shape):
     return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
 
 
-@pytest.mark.parametrize("use_graph,host_out", [(False, False), (True, False), (True, True)])
-def test_continuous_batching_loop(dev, use_graph, host_out):
+@pytest.mark.parametrize("use_graph,host_out,shared", [(False, False, False), (True, False, False),
+                                                       (True, True, False), (False, False, True),
+                                                       (True, False, True)])
+def test_continuous_batching_loop(dev, use_graph, host_out, shared):
     import torch
     import paged_kv_cache_269_gb300 as pa
     from paged_kv_cache_269_gb300.step import DecodeStep
@@ -48,7 +52,8 @@ def test_continuous_batching_loop(dev, use_graph, host_out):
     vc = torch.from_numpy(mirror_v).to(dev)
     scale = float(np.float32(1 / np.sqrt(D)))
     step = DecodeStep(kc, vc, SMAX, MB, scale, use_graph=use_graph, partition_tokens=64,
-                      host_out=host_out)
+                      host_out=host_out, max_groups=SMAX if shared else 0)
+    grouped_steps = 0
 
     def write(slots, k, v):
         """Store token K/V at slots on the device and in the mirror."""
@@ -92,8 +97,11 @@ def test_continuous_batching_loop(dev, use_graph, host_out):
                 s = mgr.add_sequence(int(rng.integers(1, 200)))
                 prefill(s, 0)
                 running.append(s)
+        batch = list(running)
+        if shared:   # sharers adjacent: by first block, stably
+            batch.sort(key=lambda s: int(mgr.block_tables([s], MB)[0][0][0]))
         slots, cow = [], []
-        for s in running:
+        for s in batch:
             slot, src, dst = mgr.append(s)
             slots.append(slot)
             if src >= 0:
@@ -102,10 +110,13 @@ def test_continuous_batching_loop(dev, use_graph, host_out):
             step.copy_on_write(cow)
             mirror_k, mirror_v = oracle.copy_blocks(mirror_k, mirror_v, mirror_k, mirror_v,
                                                     np.asarray(cow, np.int32))
-        n = len(running)
+        n = len(batch)
         q, kn, vn = (_normal(rng, (n, H, D)) for _ in range(3))
-        tables, lens = mgr.block_tables(running, MB)
-        step.prepare(q, kn, vn, np.asarray(slots, np.int32), tables, lens)
+        tables, lens = mgr.block_tables(batch, MB)
+        groups = mgr.prefix_groups(batch, SMAX) if shared else None
+        if shared and (groups[1] > 0).any():
+            grouped_steps += 1
+        step.prepare(q, kn, vn, np.asarray(slots, np.int32), tables, lens, groups=groups)
         out = step.launch()
         step.stream.synchronize()
         assert out.is_cuda != host_out              # the pinned host copy with host_out
@@ -113,7 +124,9 @@ def test_continuous_batching_loop(dev, use_graph, host_out):
         mirror_k, mirror_v = oracle.reshape_and_cache(kn, vn, mirror_k, mirror_v,
                                                       np.asarray(slots, np.int32))
         ref = oracle.decode(q, mirror_k, mirror_v, tables, lens, scale)
-        assert_parity(got, ref, f"step {it} (graph={use_graph})")
+        assert_parity(got, ref, f"step {it} (graph={use_graph}, shared={shared})")
         assert (out[n:].cpu().numpy() == 0).all()          # padding rows
     assert pa.device_errors(stream=step.stream) == 0
+    if shared:
+        assert grouped_steps >= 20                         # the prefix path was exercised
     assert np.array_equal(kc.cpu().numpy().view(np.uint16), mirror_k.view(np.uint16))

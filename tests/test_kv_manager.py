@@ -162,3 +162,91 @@ def test_padding_rows_and_errors():
     with pytest.raises(pa.PaError):
         m.free(s)
     assert m.num_free_blocks() == 8
+
+
+def _model_groups(tables, lens, B):
+    """The grouping rule, restated: row i's group prefix is what it shares with
+    row i + 1 (full blocks only); later rows join while they share at least
+    that much with row i; rows sharing nothing with the next row are gathered
+    into prefix-0 groups."""
+    n = len(lens)
+    full = [int(l) // B for l in lens]
+
+    def common(i, j):
+        c = 0
+        while c < min(full[i], full[j]) and tables[i][c] == tables[j][c]:
+            c += 1
+        return c
+
+    starts, pre, i, open0 = [], [], 0, False
+    while i < n:
+        P = common(i, i + 1) if i + 1 < n else 0
+        if P > 0:
+            j = i + 1
+            while j < n and common(i, j) >= P:
+                j += 1
+            starts.append(i)
+            pre.append(P)
+            open0, i = False, j
+        else:
+            if not open0:
+                starts.append(i)
+                pre.append(0)
+            open0, i = True, i + 1
+    return starts + [n], pre
+
+
+def test_prefix_groups_of_shared_prompts_and_forks():
+    B = 16
+    m = pa.KVManager(256, B, 32)
+    p = m.add_sequence(100)                     # 6 full blocks + a partial one
+    c1 = m.add_sequence(130, p, 6)              # shares the 6 full blocks
+    c2 = m.add_sequence(101, p, 6)
+    x = m.add_sequence(50)                      # shares nothing
+    y = m.add_sequence(70)
+    f = m.fork(c1)                              # shares all of c1, a partial block included
+    gs, gp = m.prefix_groups([p, c1, c2, x, y, c1, f, -1])
+    assert gs.tolist() == [0, 3, 5, 7, 8] and gp.tolist() == [6, 0, 8, 0]
+    # the members of each group do share those blocks, and they are full in each
+    t, l = m.block_tables([p, c1, c2, x, y, c1, f, -1], 32)
+    for g in range(len(gp)):
+        rows = range(gs[g], gs[g + 1])
+        for r in rows:
+            assert (t[r, :gp[g]] == t[gs[g], :gp[g]]).all() and gp[g] * B <= l[r]
+    es, ep = m.prefix_groups([])
+    assert es.tolist() == [0] and ep.tolist() == []
+    with pytest.raises(pa.PaError):
+        m.prefix_groups([p, c1, x, y], max_groups=1)   # needs 2 groups
+    with pytest.raises(pa.PaError):
+        m.prefix_groups([p, 999])
+
+
+def test_prefix_groups_match_the_rule(rng):
+    B = 8
+    m = pa.KVManager(4000, B, 64, shuffle_seed=3)
+    live = []
+    for _ in range(300):
+        op = rng.integers(0, 4)
+        if op == 0 or not live:
+            live.append(m.add_sequence(int(rng.integers(1, 200))))
+        elif op == 1:
+            par = live[int(rng.integers(0, len(live)))]
+            full = m.context_len(par) // B
+            k = int(rng.integers(0, full + 1))
+            live.append(m.add_sequence(k * B + int(rng.integers(0, 60)), par, k))
+        elif op == 2:
+            live.append(m.fork(live[int(rng.integers(0, len(live)))]))
+        else:
+            s = live[int(rng.integers(0, len(live)))]
+            m.append(s)
+        if len(live) > 40:
+            m.free(live.pop(int(rng.integers(0, len(live)))))
+        if rng.random() < 0.3:
+            batch = list(live)
+            rng.shuffle(batch)
+            batch.sort(key=lambda s: m.block_tables([s], 64)[0][0][0])   # sharers adjacent
+            batch += [-1] * int(rng.integers(0, 3))
+            t, l = m.block_tables(batch, 64)
+            gs, gp = m.prefix_groups(batch)
+            want_s, want_p = _model_groups(t, l, B)
+            assert gs.tolist() == want_s and gp.tolist() == want_p

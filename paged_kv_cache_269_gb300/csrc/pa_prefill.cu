@@ -342,13 +342,15 @@ __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu
 struct Item {
     int s, h, row0, q_first, q_len, ctx, ntiles, kmax, nkt;
     int table_row;   // block-table row of the keys
-    bool causal;     // false: every row sees keys 0 .. ctx - 1 (shared-prefix mode)
 };
 
 // Work item w, heaviest pairs (latest positions) first: w = (level, s, h)
 // with pair = num_pairs - 1 - level.  Returns false for an empty item (the
 // sequence has no query rows in that pair) or, with `check`, for a sequence
 // whose lengths are inconsistent (recorded in the error word).
+// kShared: shared-prefix mode (a compile-time variant of the kernel, so the
+// causal kernel carries none of its tests).
+template <bool kShared>
 __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool check, Item &it) {
     const int sh = a.num_seqs * a.num_heads;
     const int level = w / sh;
@@ -362,7 +364,7 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
     const bool rows_bad = it.q_first < 0 || q_end < it.q_first || q_end > a.total_q;
     it.q_len = rows_bad ? 0 : q_end - it.q_first;
     it.row0 = pair * kTiles * kBM;
-    if (a.group_prefix_blocks != nullptr) {
+    if constexpr (kShared) {
         // shared-prefix mode: s is a group of decode rows, all of which see
         // the whole prefix through the group's first row's table.  A
         // malformed group is skipped here; the plan kernel reports it and
@@ -373,7 +375,6 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
             return false;
         it.ctx = pb * kB;
         it.table_row = it.q_first;
-        it.causal = false;
         it.ntiles = it.q_len - it.row0 > kBM ? 2 : 1;
         it.kmax = it.ctx;
         it.nkt = (it.kmax + kBN - 1) / kBN;
@@ -381,7 +382,6 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
     }
     it.ctx = __ldg(a.context_lens + it.s);
     it.table_row = it.s;
-    it.causal = true;
     // query rows past num_pairs * 256 (max_query_len understated) would never be
     // computed: reported once per sequence
     if (check && it.h == 0 && it.row0 == 0 && it.q_len > a.num_pairs * kTiles * kBM)
@@ -399,14 +399,15 @@ __device__ __forceinline__ bool item_geometry(const PrefillArgs &a, int w, bool 
 }
 
 // key tiles needed by query tile t of an item (0 if the tile is idle)
+template <bool kShared>
 __device__ __forceinline__ int tile_key_tiles(const Item &it, int t) {
     if (t >= it.ntiles) return 0;
-    if (!it.causal) return it.nkt;
+    if constexpr (kShared) return it.nkt;
     const int rows_t = min(kBM, it.q_len - it.row0 - t * kBM);
     return (it.ctx - it.q_len + it.row0 + t * kBM + rows_t + kBN - 1) / kBN;
 }
 
-template <typename E>
+template <typename E, bool kShared>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) w = static_cast<int>(atomicAdd(a.counters, 1u));
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (w >= num_items) break;
-                if (item_geometry(a, w, lane == 0, it)) break;
+                if (item_geometry<kShared>(a, w, lane == 0, it)) break;
             }
             const bool done = w >= num_items;
             const int slot = k % 2;
@@ -591,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bar[ITEM_EMPTY + slot]);
                 if (w < 0) break;
                 Item it;
-                item_geometry(a, w, false, it);
-                const int nk = tile_key_tiles(it, t);
+                item_geometry<kShared>(a, w, false, it);
+                const int nk = tile_key_tiles<kShared>(it, t);
                 ok = mbar_wait(&bar[Q_FULL], k & 1, abort_flag, a.err);
                 if (ok && nk == 0) mbar_arrive(&bar[Q_EMPTY]);   // this query tile is idle
                 for (int j = 0; j < it.nkt && ok; ++j, ++g) {
@@ -652,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bar[ITEM_EMPTY + slot]);
                 if (w < 0) break;
                 Item it;
-                item_geometry(a, w, false, it);
-                const int nk = tile_key_tiles(it, t);
+                item_geometry<kShared>(a, w, false, it);
+                const int nk = tile_key_tiles<kShared>(it, t);
                 for (int j = 0; j < it.nkt && ok; ++j, ++g) {
                     const int st = g % kStages;
                     const bool last = j == it.nkt - 1;
@@ -715,14 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bar[ITEM_EMPTY + slot]);
             if (w < 0) break;
             Item it;
-            item_geometry(a, w, false, it);
+            item_geometry<kShared>(a, w, false, it);
             if (t >= it.ntiles) continue;
             const int rows_t = min(kBM, it.q_len - it.row0 - t * kBM);
             // key position of the row (every row sits past the whole prefix
             // in shared-prefix mode)
-            const int first_pos = it.causal ? it.ctx - it.q_len + it.row0 + t * kBM : it.ctx - 1;
-            const int my_nkt = tile_key_tiles(it, t);
-            const int pos = r < rows_t ? (it.causal ? first_pos + r : first_pos) : -1;   // -1: padding row, all masked
+            const int first_pos = kShared ? it.ctx - 1 : it.ctx - it.q_len + it.row0 + t * kBM;
+            const int my_nkt = tile_key_tiles<kShared>(it, t);
+            const int pos = r < rows_t ? (kShared ? first_pos : first_pos + r) : -1;   // -1: padding row, all masked
             const int warp_min_pos = __reduce_min_sync(0xffffffffu, pos);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < my_nkt && ok; ++j, ++n) {
@@ -850,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[O_EMPTY + t]);
-            if (r < rows_t && a.group_prefix_blocks != nullptr) {
+            if (kShared && r < rows_t) {
                 // a decode partial for row s: the weights were 2^(x - (m - 6))
                 const size_t pidx =
                     (static_cast<size_t>(it.q_first + it.row0 + t * kBM + r) * H + it.h) * a.max_parts;
@@ -937,21 +938,27 @@ cudaError_t launch_prefill(const PrefillArgs &args, const void *q, const void *k
         !encode(&tm_k, bf16, k_cache, 2, kv_dims, kv_strides, kv_box) ||
         !encode(&tm_v, bf16, v_cache, 2, kv_dims, kv_strides, kv_box))
         return cudaErrorInvalidValue;
-    const void *kernel = bf16 ? reinterpret_cast<const void *>(&prefill_kernel<BF16T>)
-                              : reinterpret_cast<const void *>(&prefill_kernel<F16T>);
+    const bool shared = args.group_prefix_blocks != nullptr;
+    const void *kernels[2][2] = {
+        {reinterpret_cast<const void *>(&prefill_kernel<F16T, false>),
+         reinterpret_cast<const void *>(&prefill_kernel<F16T, true>)},
+        {reinterpret_cast<const void *>(&prefill_kernel<BF16T, false>),
+         reinterpret_cast<const void *>(&prefill_kernel<BF16T, true>)}};
+    const void *kernel = kernels[bf16 ? 1 : 0][shared ? 1 : 0];
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     {
         static std::mutex mu;
-        static bool ready[64][2] = {};
+        static bool ready[64][4] = {};   // per kernel variant
+        const int which = (bf16 ? 2 : 0) + (shared ? 1 : 0);
         std::lock_guard<std::mutex> lock(mu);
-        if (!ready[device][bf16 ? 1 : 0]) {
+        if (!ready[device][which]) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kSmemBytes);
             if (e != cudaSuccess) return e;
-            ready[device][bf16 ? 1 : 0] = true;
+            ready[device][which] = true;
         }
     }
     void *params[] = {&tm_q, &tm_k, &tm_v, const_cast<PrefillArgs *>(&args)};

@@ -118,6 +118,33 @@ def recorded_prefill_traffic(workload):
         return None
 
 
+SHARED_SOURCES = DECODE_SOURCES + PREFILL_SOURCES
+
+
+def recorded_shared_traffic():
+    """DRAM bytes (read + write) of one shared-prefix call (the prefix kernel
+    plus the suffix decode) from the committed ncu summary, if it was taken on
+    the current sources of both kernels; else None."""
+    path = os.path.join(ROOT, "profiles", "pa_decode_shared_prefix.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path, encoding="utf-8"):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for rel in SHARED_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if vals.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_call"]))
+    except (KeyError, ValueError):
+        return None
+
+
 def recorded_traffic(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
@@ -779,7 +806,8 @@ def run_shared_prefix_op(args, local_rank):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": "prefix kernel + suffix decode (two launches)",
                      "unique_bytes_per_call": int(uniq), "logical_bytes_per_call": int(logical),
-                     "traffic": None},
+                     "traffic": recorded_shared_traffic(),
+                     "traffic_unit": "DRAM bytes per call (both kernels)"},
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(t_begin, t_end) if sampler else None}))
 

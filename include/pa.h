@@ -151,7 +151,11 @@ int pa_copy_blocks(const void *src_k, const void *src_v, int32_t src_num_blocks,
  * (mjmagnets.cn vLLM tutorial, §2.2; "vLLM 2026 推理引擎全解", §2.2, where the
  * attention is computed page by page as a paged extension of FlashAttention).
  *
- *   out           device, fp16 [S, H, D]: written
+ *   out           device, fp16 [S, H, D]: written.  It may also be pinned or
+ *                 registered host memory (the output rows then go straight to
+ *                 the host over the host link, written by the kernel as each
+ *                 row completes); the caller reads it after the stream has
+ *                 reached the end of the call
  *   q             device, fp16 [S, H, D]: one query per sequence and head
  *   k_cache       device, fp16 [N, H, B, D]
  *   v_cache       device, fp16 [N, H, B, D]

@@ -188,6 +188,19 @@ def _need(t, name, dtype, ndim, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _need_out(t, et, ndim, device):
+    """The output of a decode: a CUDA tensor on `device`, or pinned host
+    memory, which the kernel then writes directly over the host link."""
+    torch = _torch()
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError("out must be a CUDA tensor or pinned host memory")
+        if t.dtype != et or t.dim() != ndim or not t.is_contiguous():
+            raise ValueError(f"out must be a contiguous {ndim}-d tensor of {et}")
+        return
+    _need(t, "out", et, ndim, device)
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
@@ -408,7 +421,8 @@ def reset_workspaces():
 def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
            max_blocks_per_seq=None, partition_tokens=0, workspace=None, counters=None,
            stream=None, allocate_in_library=False):
-    """Paged-attention decode into `out` [S, H, D].
+    """Paged-attention decode into `out` [S, H, D] (a CUDA tensor, or pinned
+    host memory that the kernel writes directly).
 
     q [S, H, D]; k_cache / v_cache [N, H, B, D], all float16 or all
     bfloat16; block_tables
@@ -426,7 +440,7 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
     dev = k_cache.device
     _need(v_cache, "v_cache", et, 4, dev)
     _need(q, "q", et, 3, dev)
-    _need(out, "out", et, 3, dev)
+    _need_out(out, et, 3, dev)
     _need(block_tables, "block_tables", torch.int32, 2, dev)
     _need(context_lens, "context_lens", torch.int32, 1, dev)
     N, H, B, D = k_cache.shape
@@ -488,7 +502,7 @@ def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, s
     dev = k_cache.device
     _need(v_cache, "v_cache", et, 4, dev)
     _need(q, "q", et, 3, dev)
-    _need(out, "out", et, 3, dev)
+    _need_out(out, et, 3, dev)
     _need(block_tables, "block_tables", torch.int32, 2, dev)
     _need(context_lens, "context_lens", torch.int32, 1, dev)
     _need(group_start, "group_start", torch.int32, 1, dev)

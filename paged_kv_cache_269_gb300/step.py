@@ -67,10 +67,12 @@ class DecodeStep:
         self.d = {n: self.devbuf[o:o + nb].view(td).view(shape) for n, (o, shape, nd, td, nb)
                   in self.layout.items()}
         self.out = torch.zeros((S, H, D), dtype=self.dtype, device=self.dev)
-        # with host_out, the step ends by copying the output into pinned host
-        # memory (part of the graph), read it after the stream reaches it
+        # with host_out, the decode writes its output straight into pinned
+        # host memory over the host link (no separate copy); read it after
+        # the stream reaches the end of the step
         self.out_host = (torch.empty((S, H, D), dtype=self.dtype).pin_memory()
                          if host_out else None)
+        self.dst = self.out_host if host_out else self.out
         dt = 1 if self.dtype == torch.bfloat16 else 0
         if self.G > 0:
             ws = decode_shared_prefix_workspace_bytes(S, H, D, B, N, MB, partition_tokens, dtype=dt)
@@ -123,16 +125,14 @@ class DecodeStep:
         self.devbuf.copy_(self.host, non_blocking=True)
         reshape_and_cache(d["k_new"], d["v_new"], self.k_cache, self.v_cache, d["slots"])
         if self.G > 0:
-            decode_shared_prefix(self.out, d["q"], self.k_cache, self.v_cache, d["tables"],
+            decode_shared_prefix(self.dst, d["q"], self.k_cache, self.v_cache, d["tables"],
                                  d["lens"], self.scale, d["gstart"], d["gpre"],
                                  max_group_size=self.S, partition_tokens=self.partition_tokens,
                                  workspace=self.workspace, counters=self.counters)
         else:
-            decode(self.out, d["q"], self.k_cache, self.v_cache, d["tables"], d["lens"],
+            decode(self.dst, d["q"], self.k_cache, self.v_cache, d["tables"], d["lens"],
                    self.scale, partition_tokens=self.partition_tokens, workspace=self.workspace,
                    counters=self.counters)
-        if self.out_host is not None:
-            self.out_host.copy_(self.out, non_blocking=True)
 
     def copy_on_write(self, pairs):
         """Make the manager's copy-on-write copies ((src, dst) rows) before the step."""

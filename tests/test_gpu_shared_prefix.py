@@ -208,3 +208,52 @@ def test_malformed_group_arrays(dev, bad):
     else:
         gp[0] = case.max_blocks_per_seq + 1
     _expect_full_decode(dev, case, gs, gp, bad, max_group_size=int(np.abs(np.diff(gs)).max()))
+
+
+def test_no_groups_is_plain_decode_bit_for_bit(dev):
+    """With no group (or max_group_size 0) the call is pa_decode itself."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    rng = np.random.default_rng(3)
+    case, gs, gp = workloads.build_grouped_case("nogroups", _layout(rng)[:3], num_heads=2,
+                                                head_dim=128, seed=3)
+    d = upload(case, dev)
+    plain = torch.empty(case.q.shape, dtype=torch.float16, device=dev)
+    pa.decode(plain, d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+              case.scale, partition_tokens=256)
+    for g_start, g_pre, mgs in ((np.zeros(1, np.int32), np.zeros(0, np.int32), 0), (gs, gp, 0)):
+        out = torch.full_like(plain, float("nan"))
+        pa.decode_shared_prefix(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                d["context_lens"], case.scale, torch.from_numpy(g_start).to(dev),
+                                torch.from_numpy(g_pre).to(dev), max_group_size=mgs,
+                                partition_tokens=256)
+        assert pa.device_errors() == 0
+        assert torch.equal(out.view(torch.int16), plain.view(torch.int16))
+
+
+def test_output_in_pinned_host_memory(dev):
+    """out may be pinned host memory: the decode kernel writes the rows there
+    directly; the result equals the device-memory output bit for bit."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    rng = np.random.default_rng(4)
+    case, gs, gp = workloads.build_grouped_case("hostout", _layout(rng)[:4], num_heads=2,
+                                                head_dim=128, seed=4)
+    d = upload(case, dev)
+    g_start, g_pre = torch.from_numpy(gs).to(dev), torch.from_numpy(gp).to(dev)
+    on_dev = torch.empty(case.q.shape, dtype=torch.float16, device=dev)
+    on_host = torch.full(case.q.shape, float("nan"), dtype=torch.float16).pin_memory()
+    for out in (on_dev, on_host):
+        pa.decode_shared_prefix(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                d["context_lens"], case.scale, g_start, g_pre)
+    plain_host = torch.full(case.q.shape, float("nan"), dtype=torch.float16).pin_memory()
+    pa.decode(plain_host, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+              d["context_lens"], case.scale)
+    torch.cuda.synchronize(dev)
+    assert pa.device_errors() == 0
+    assert torch.equal(on_host.view(torch.int16), on_dev.cpu().view(torch.int16))
+    assert_parity(on_host.numpy(), oracle.decode_case(case), "shared prefix, host output")
+    assert_parity(plain_host.numpy(), oracle.decode_case(case), "plain decode, host output")
+    with pytest.raises(ValueError):        # pageable host memory is refused
+        pa.decode(torch.empty(case.q.shape, dtype=torch.float16), d["q"], d["k_cache"],
+                  d["v_cache"], d["block_tables"], d["context_lens"], case.scale)

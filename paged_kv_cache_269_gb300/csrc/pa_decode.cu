@@ -59,6 +59,7 @@ constexpr int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? 
 #ifndef PA_DECODE_MAX_STAGES
 #define PA_DECODE_MAX_STAGES 16
 #endif
+
 #ifndef PA_DECODE_MIXED_FMA
 #define PA_DECODE_MIXED_FMA 1
 #endif
@@ -75,7 +76,14 @@ struct Cfg {
     static constexpr int TILE_BYTES = B * D * 2;      // one K (or V) tile, fp16
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int STAGE_BUDGET = PA_DECODE_STAGE_KIB * 1024;
-    static constexpr int NS = clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, PA_DECODE_MAX_STAGES);
+    // At least 4 stages, unless a 4-stage ring of very large tiles would
+    // exceed twice the budget (D 256 x B 32: 128 KiB, one CTA per SM); then
+    // 3 stages, so that two CTAs fit (0.91 -> 0.985 of the copy rate there,
+    // while 3 stages cost 2 % on the 16 KiB tiles).
+    static constexpr int NS_WANT = clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, PA_DECODE_MAX_STAGES);
+    static constexpr int NS = NS_WANT * STAGE_BYTES > 2 * STAGE_BUDGET
+                                  ? clamp_int(2 * STAGE_BUDGET / STAGE_BYTES, 3, PA_DECODE_MAX_STAGES)
+                                  : NS_WANT;
     static constexpr int ND = PA_DECODE_DESC_SLOTS;   // unit descriptor slots
     // q.k layout: LPT lanes per token, 8 dims (16 bytes) per lane.
     static constexpr int LPT = D / 8;

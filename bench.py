@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--op", choices=["step", "copy_blocks", "swap_out", "swap_in", "prefill",
-                                    "shared_prefix"],
+                                    "shared_prefix", "variants"],
                    default="step",
                    help="step: reshape_and_cache + decode (the hot path); the others time "
                         "pa_copy_blocks on a 4096-block pool, 2048 random pairs")
@@ -812,6 +812,63 @@ def run_shared_prefix_op(args, local_rank):
         "clocks": sampler.summary(t_begin, t_end) if sampler else None}))
 
 
+def run_variants_op(args, local_rank):
+    """Decode GB/s of every built (dtype, head_dim, block_size) variant on a
+    LLaMA-shaped batch with the same bytes per token (64 sequences, contexts
+    U[128, 2048], H x D = 4096): decode only, --steps launches between two
+    events, against the measured copy rate.  One JSON line."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pa.lib()
+    peak, peak_kind = measured_peaks()
+    rng = np.random.default_rng(11)
+    ctx = rng.integers(128, 2049, size=64)
+    steps = max(1, args.steps)
+    results = []
+    for dt in ("f16", "bf16"):
+        for D in (64, 128, 256):
+            for B in (8, 16, 32):
+                H = 4096 // D
+                case = workloads.build_case(f"v{D}_{B}", ctx, num_heads=H, head_dim=D,
+                                            block_size=B, seed=31, dtype=dt)
+
+                def t(a):
+                    a = np.ascontiguousarray(a)
+                    if a.dtype == np.uint16:
+                        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+                    return torch.from_numpy(a).to(dev)
+
+                q, kc, vc, bt, cl = map(t, (case.q, case.k_cache, case.v_cache, case.block_tables,
+                                            case.context_lens))
+                out = torch.empty_like(q)
+                stream = torch.cuda.Stream(dev)
+                for _ in range(max(3, args.warmup)):
+                    pa.decode(out, q, kc, vc, bt, cl, case.scale, stream=stream)
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(steps):
+                    pa.decode(out, q, kc, vc, bt, cl, case.scale, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                if pa.device_errors(stream=stream):
+                    raise RuntimeError(f"device error in variant {dt} {D}x{B}")
+                us = e0.elapsed_time(e1) / steps * 1e3
+                gbs = workloads.decode_algorithmic_bytes(case) / us / 1e3
+                results.append({"dtype": dt, "head_dim": D, "block_size": B, "num_heads": H,
+                                "decode_us": round(us, 2), "GB/s": round(gbs, 1),
+                                "frac": round(gbs / peak, 4)})
+                del q, kc, vc, bt, cl, out, case
+                torch.cuda.empty_cache()
+    print(json.dumps({"metric": "pa_decode GB/s per variant", "unit": "GB/s",
+                      "steps": steps, "warmup": max(3, args.warmup), "data": "synthetic",
+                      "config": {"num_seqs": 64, "context": "U[128, 2048]", "heads_x_dim": 4096,
+                                 "launches": "decode only, between two events"},
+                      "peak": peak, "peak_source": peak_kind, "variants": results}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -827,6 +884,10 @@ def main():
     if args.op == "shared_prefix":
         if rank == 0:
             run_shared_prefix_op(args, local_rank)
+        return
+    if args.op == "variants":
+        if rank == 0:
+            run_variants_op(args, local_rank)
         return
     if args.op != "step":
         if rank == 0:

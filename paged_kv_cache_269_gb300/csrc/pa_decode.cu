@@ -74,13 +74,20 @@ struct Cfg {
     static constexpr int NC = PA_DECODE_CONSUMER_WARPS;  // consumer warps
     static constexpr int THREADS = (NC + 1) * 32;     // + one producer warp
     static constexpr int TILE_BYTES = B * D * 2;      // one K (or V) tile, fp16
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    // Blocks per ring stage: tiles under 2 KiB (D 64 x B 8) are grouped four to
+    // a stage, so that one barrier, tag and hand-off carries 4 KiB of K and of
+    // V; every other shape keeps one block per stage.
+    static constexpr int R = TILE_BYTES < 2048 ? 4096 / TILE_BYTES : 1;
+    static_assert(32 % R == 0, "a stage never straddles a 32-entry table slice");
+    static constexpr int STAGE_BYTES = 2 * R * TILE_BYTES;  // [K tiles][V tiles]
     static constexpr int STAGE_BUDGET = PA_DECODE_STAGE_KIB * 1024;
     // At least 4 stages, unless a 4-stage ring of very large tiles would
     // exceed twice the budget (D 256 x B 32: 128 KiB, one CTA per SM); then
     // 3 stages, so that two CTAs fit (0.91 -> 0.985 of the copy rate there,
     // while 3 stages cost 2 % on the 16 KiB tiles).
-    static constexpr int NS_WANT = clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, PA_DECODE_MAX_STAGES);
+    // (the ring holds at most PA_DECODE_MAX_STAGES blocks)
+    static constexpr int NS_WANT =
+        clamp_int(STAGE_BUDGET / STAGE_BYTES, 4, PA_DECODE_MAX_STAGES / R);
     static constexpr int NS = NS_WANT * STAGE_BYTES > 2 * STAGE_BUDGET
                                   ? clamp_int(2 * STAGE_BUDGET / STAGE_BYTES, 3, PA_DECODE_MAX_STAGES)
                                   : NS_WANT;
@@ -640,27 +647,68 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
             for (int j0 = 0; j0 < nt && ok; j0 += 32) {
                 const int n = min(32, nt - j0);
                 const int phys_lane = lane < n ? __ldg(row + j0 + lane) : 0;
-                for (int jj = 0; jj < n; ++jj) {
-                    const int phys = __shfl_sync(kFull, phys_lane, jj);
-                    const int st = static_cast<int>(kq % C::NS);
-                    w_ok = mbar_wait(&empty[st], ((kq / C::NS) & 1u) ^ 1u, abort_flag, a.err);
-                    if (!__all_sync(kFull, w_ok)) { ok = false; break; }
-                    if (lane == 0) {
-                        const bool in_pool = static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks);
-                        stage_ok[st] = in_pool ? 1 : 0;
-                        stage_tag[st] = kq;
-                        if (in_pool) {
-                            const size_t off = (static_cast<size_t>(phys) * H + h) * (B * D);
-                            uint8_t *dst = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
-                            mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES);
-                            bulk_copy_g2s(dst, a.k_cache + off, C::TILE_BYTES, &full[st]);
-                            bulk_copy_g2s(dst + C::TILE_BYTES, a.v_cache + off, C::TILE_BYTES, &full[st]);
-                        } else {
-                            atomicOr(a.err, PA_DEVERR_TABLE);
-                            mbar_arrive(&full[st]);
+                if constexpr (C::R == 1) {
+                    for (int jj = 0; jj < n; ++jj) {
+                        const int phys = __shfl_sync(kFull, phys_lane, jj);
+                        const int st = static_cast<int>(kq % C::NS);
+                        w_ok = mbar_wait(&empty[st], ((kq / C::NS) & 1u) ^ 1u, abort_flag, a.err);
+                        if (!__all_sync(kFull, w_ok)) { ok = false; break; }
+                        if (lane == 0) {
+                            const bool in_pool = static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks);
+                            stage_ok[st] = in_pool ? 1 : 0;
+                            stage_tag[st] = kq;
+                            if (in_pool) {
+                                const size_t off = (static_cast<size_t>(phys) * H + h) * (B * D);
+                                uint8_t *dst = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
+                                mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES);
+                                bulk_copy_g2s(dst, a.k_cache + off, C::TILE_BYTES, &full[st]);
+                                bulk_copy_g2s(dst + C::TILE_BYTES, a.v_cache + off, C::TILE_BYTES, &full[st]);
+                            } else {
+                                atomicOr(a.err, PA_DEVERR_TABLE);
+                                mbar_arrive(&full[st]);
+                            }
                         }
+                        ++kq;
                     }
-                    ++kq;
+                } else {
+                    for (int jj = 0; jj < n; jj += C::R) {   // one stage: blocks jj .. jj + R - 1
+                        int phys[C::R];
+#pragma unroll
+                        for (int r = 0; r < C::R; ++r) phys[r] = __shfl_sync(kFull, phys_lane, jj + r);
+                        const int st = static_cast<int>(kq % C::NS);
+                        w_ok = mbar_wait(&empty[st], ((kq / C::NS) & 1u) ^ 1u, abort_flag, a.err);
+                        if (!__all_sync(kFull, w_ok)) { ok = false; break; }
+                        if (lane == 0) {
+                            // bit r: block jj + r exists and is in the pool (copied)
+                            uint32_t mask = 0;
+#pragma unroll
+                            for (int r = 0; r < C::R; ++r) {
+                                if (jj + r >= n) break;
+                                if (static_cast<unsigned>(phys[r]) < static_cast<unsigned>(a.num_blocks))
+                                    mask |= 1u << r;
+                                else
+                                    atomicOr(a.err, PA_DEVERR_TABLE);
+                            }
+                            stage_ok[st] = static_cast<int>(mask);
+                            stage_tag[st] = kq;
+                            if (mask) {
+                                uint8_t *dst = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
+                                mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES * __popc(mask));
+#pragma unroll
+                                for (int r = 0; r < C::R; ++r) {
+                                    if (!(mask & (1u << r))) continue;
+                                    const size_t off = (static_cast<size_t>(phys[r]) * H + h) * (B * D);
+                                    bulk_copy_g2s(dst + r * C::TILE_BYTES, a.k_cache + off, C::TILE_BYTES,
+                                                  &full[st]);
+                                    bulk_copy_g2s(dst + (C::R + r) * C::TILE_BYTES, a.v_cache + off,
+                                                  C::TILE_BYTES, &full[st]);
+                                }
+                            } else {
+                                mbar_arrive(&full[st]);
+                            }
+                        }
+                        ++kq;
+                    }
                 }
             }
             if (!ok) break;
@@ -732,23 +780,48 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
 #pragma unroll
         for (int i = 0; i < C::DPL; ++i) acc[i] = 0.f;
 
-        for (int j = w; j < nt; j += C::NC) {
-            const uint32_t k = kq + j;
-            const int st = static_cast<int>(k % C::NS);
-            w_ok = wait_value(&stage_tag[st], k, abort_flag, a.err) &&
-                   mbar_wait(&full[st], (k / C::NS) & 1u, abort_flag, a.err);
-            if (!__all_sync(kFull, w_ok)) return;
-            if (stage_ok[st]) {
-                const int tok0 = (t0 + j) * B;
-                const int nvalid = min(B, ctx - tok0);
-                const uint8_t *ktile = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
-                consume_tile<E, D, B>(ktile, ktile + C::TILE_BYTES, qraw, qf, a.scale_log2, nvalid,
-                                   run_max, run_sum, acc, probs, lane);
+        if constexpr (C::R == 1) {
+            for (int j = w; j < nt; j += C::NC) {
+                const uint32_t k = kq + j;
+                const int st = static_cast<int>(k % C::NS);
+                w_ok = wait_value(&stage_tag[st], k, abort_flag, a.err) &&
+                       mbar_wait(&full[st], (k / C::NS) & 1u, abort_flag, a.err);
+                if (!__all_sync(kFull, w_ok)) return;
+                if (stage_ok[st]) {
+                    const int tok0 = (t0 + j) * B;
+                    const int nvalid = min(B, ctx - tok0);
+                    const uint8_t *ktile = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
+                    consume_tile<E, D, B>(ktile, ktile + C::TILE_BYTES, qraw, qf, a.scale_log2,
+                                          nvalid, run_max, run_sum, acc, probs, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            kq += nt;
+        } else {
+            const int nstages = (nt + C::R - 1) / C::R;   // ring stages of this unit
+            for (int j = w; j < nstages; j += C::NC) {
+                const uint32_t k = kq + j;
+                const int st = static_cast<int>(k % C::NS);
+                w_ok = wait_value(&stage_tag[st], k, abort_flag, a.err) &&
+                       mbar_wait(&full[st], (k / C::NS) & 1u, abort_flag, a.err);
+                if (!__all_sync(kFull, w_ok)) return;
+                const uint32_t mask = static_cast<uint32_t>(stage_ok[st]);
+                const uint8_t *stage = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
+#pragma unroll
+                for (int r = 0; r < C::R; ++r) {
+                    if (!(mask & (1u << r))) continue;   // past the unit, or outside the pool
+                    const int tok0 = (t0 + j * C::R + r) * B;
+                    const int nvalid = min(B, ctx - tok0);
+                    consume_tile<E, D, B>(stage + r * C::TILE_BYTES,
+                                          stage + (C::R + r) * C::TILE_BYTES, qraw, qf,
+                                          a.scale_log2, nvalid, run_max, run_sum, acc, probs, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+            kq += nstages;
         }
-        kq += nt;
 
         // hand this warp's state to the unit's owner warp
         store_f32<C::DPL>(merge_acc + (slot * C::NC + w) * D + lane * C::DPL, acc);

@@ -207,7 +207,7 @@ class ClockSampler:
         if self.thread:
             self.thread.join(timeout=5)
 
-    def summary(self, t0, t1):
+    def summary(self, t0, t1, window="timed region"):
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         import datetime
@@ -232,7 +232,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm), "window": "timed region"}
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
 # ----------------------------------------------------------------------------
@@ -361,7 +361,8 @@ def config_of(case, args):
 # native leg
 # ----------------------------------------------------------------------------
 
-EVENT_EVERY = 8   # steps per sampled decode duration
+ROOFLINE_MIN_LAUNCHES = 200     # decode-only launches timed for the roofline
+ROOFLINE_MIN_SECONDS = 0.5      # ... and at least this long, so the clock sampler sees it
 
 
 def run_native(args, rank, world, local_rank):
@@ -395,46 +396,47 @@ def run_native(args, rank, world, local_rank):
 
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
 
+    def decode_only(ins):
+        pa.decode(out, ins["q"], d["k_cache"], d["v_cache"], ins["block_tables"],
+                  ins["context_lens"], case.scale, partition_tokens=args.partition_tokens,
+                  workspace=ws, counters=ctr, stream=stream)
+
     def step(ins, ev=None):
         if flush_buf is not None:
             with torch.cuda.stream(stream):
                 flush_buf.fill_(1)
-        if ev is not None and len(ev) > 2:
+        if ev is not None:
             ev[2].record(stream)
         pa.reshape_and_cache(ins["k_new"], ins["v_new"], d["k_cache"], d["v_cache"],
                              ins["slot_mapping"], stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        pa.decode(out, ins["q"], d["k_cache"], d["v_cache"], ins["block_tables"],
-                  ins["context_lens"], case.scale, partition_tokens=args.partition_tokens,
-                  workspace=ws, counters=ctr, stream=stream)
+        decode_only(ins)
         if ev is not None:
             ev[1].record(stream)
 
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    # The clock sampler starts before the warm-up, so that its start-up pause
+    # never leaves the GPU idle between the warm-up and the timed steps.
+    sampler = ClockSampler(local_rank) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     for _ in range(max(3, args.warmup)):
         step(d)
     torch.cuda.synchronize(dev)
     if pa.device_errors(stream=stream):
         raise RuntimeError("device error during warm-up")
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-    nev = 3 if args.flush_l2 else 2
-    # The decode's duration is sampled with events around it on every
-    # EVENT_EVERY-th step: an event between the two kernels keeps the decode
-    # from launching early, so the other steps run without them.  (With
-    # --flush-l2 every step needs its events: the step time is built from
-    # them.)
-    every = 1 if args.flush_l2 else EVENT_EVERY
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(nev)) if i % every == 0
-           else None for i in range(args.steps)]
+    # With --flush-l2 every step carries events around its kernels (the step
+    # time is built from them, flush excluded); otherwise the K steps run with
+    # no event between their kernels, so each decode may launch early.
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+           for _ in range(args.steps)] if args.flush_l2 else [None] * args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank) if not args.no_clocks else None
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -444,19 +446,51 @@ def run_native(args, rank, world, local_rank):
         step(d, evs[i])
     end.record(stream)
     torch.cuda.synchronize(dev)
+    step_ms = start.elapsed_time(end) / args.steps
+    if args.flush_l2:  # per-step events around reshape + decode, flush excluded
+        step_ms = sum(e[2].elapsed_time(e[1]) for e in evs) / args.steps
+    if pa.device_errors(stream=stream):
+        raise RuntimeError("device error during the timed steps")
+
+    # The decode kernel's own duration, for the roofline: right after the
+    # steps, back-to-back decode launches between two events on the launching
+    # stream, at least ROOFLINE_MIN_LAUNCHES of them and at least
+    # ROOFLINE_MIN_SECONDS.  With --flush-l2, every decode of the timed steps
+    # was bracketed by events after a flush; their mean is used instead.
+    if args.flush_l2:
+        decode_ms_each = [e[0].elapsed_time(e[1]) for e in evs]
+        decode_ms = sum(decode_ms_each) / len(decode_ms_each)
+        n_roof = len(decode_ms_each)
+        sampling = (f"CUDA events around the decode of each of the {n_roof} timed steps, "
+                    f"L2 flushed before each step")
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            decode_only(d)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        est_ms = e0.elapsed_time(e1) / 20
+        n_roof = max(ROOFLINE_MIN_LAUNCHES, int(ROOFLINE_MIN_SECONDS * 1e3 / max(est_ms, 1e-3)) + 1)
+        n_roof = min(n_roof, 200000)
+        e0.record(stream)
+        for _ in range(n_roof):
+            decode_only(d)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        decode_ms = e0.elapsed_time(e1) / n_roof
+        decode_ms_each = [decode_ms]
+        sampling = (f"{n_roof} back-to-back decode launches between two CUDA events on the "
+                    f"launching stream, right after the timed steps "
+                    f"({decode_ms * n_roof / 1e3:.2f} s)")
     t_end = time.time()
     if dist:
         dist.barrier()
     if sampler:
         time.sleep(0.1)
         sampler.stop()
-    step_ms = start.elapsed_time(end) / args.steps
-    if args.flush_l2:  # per-step events around reshape + decode, flush excluded
-        step_ms = sum(e[2].elapsed_time(e[1]) for e in evs) / args.steps
-    decode_ms_each = [e[0].elapsed_time(e[1]) for e in evs if e is not None]
-    decode_ms = sum(decode_ms_each) / len(decode_ms_each)
     if pa.device_errors(stream=stream):
-        raise RuntimeError("device error during the timed steps")
+        raise RuntimeError("device error during the roofline launches")
 
     # e2e: per-step inputs from pinned host memory, result read back every step
     e2e = None
@@ -549,15 +583,13 @@ def run_native(args, rank, world, local_rank):
         "tokens_per_s": round(world * case.num_seqs / (step_ms * 1e-3), 1),
         "pct_of_peak": round(100 * value / peak, 2),
         "decode_ms": round(decode_ms, 4),
-        "decode_ms_median": round(statistics.median(decode_ms_each), 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": "pa_decode",
-                     "duration_sampling": f"CUDA events around the decode on every "
-                                          f"{1 if args.flush_l2 else EVENT_EVERY}-th timed step "
-                                          f"({len(decode_ms_each)} launches)",
+                     "duration_sampling": sampling,
+                     "launches_timed": int(n_roof),
                      "algorithmic_bytes_per_launch": int(dec_bytes),
                      "unique_bytes_per_launch": int(uniq_bytes),
                      "achieved_unique": round(uniq_bytes / (decode_ms * 1e-3) / 1e9, 2),
@@ -565,7 +597,8 @@ def run_native(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
-        "clocks": sampler.summary(t_begin, t_end) if sampler else None,
+        "clocks": sampler.summary(t_begin, t_end, "timed steps and the decode launches timed "
+                                  "for the roofline") if sampler else None,
     }
     print(json.dumps(line))
 

@@ -27,6 +27,11 @@
  *    recorded in a per-device error word, read with pa_device_errors(); the
  *    kernels skip the offending access instead of faulting.
  *  - No call aborts, throws or traps.
+ *  - The library caches per-device state on first use (device addresses of
+ *    its error word and scratch array, kernel attributes).  A
+ *    cudaDeviceReset, or anything else that destroys the device's primary
+ *    context, invalidates that state: the library must not be called on that
+ *    device afterwards within the same process.
  */
 #ifndef PA_H
 #define PA_H
@@ -392,6 +397,9 @@ int pa_decode_shared_prefix(void *out, const void *q, const void *k_cache, const
  *   Partition length: the pa_decode default when its partial results fit in
  *   the array, otherwise the smallest power-of-two multiple of 512 tokens
  *   that fits, or one pass over each whole context (no partials).
+ *   Checks: every argument check (NULL pointers, alignment, sizes, a
+ *   non-finite scale, the limit below) runs before the set-up and the
+ *   memset, so a rejected call touches no device and launches nothing.
  *   Limits: returns PA_ERR_WORKSPACE, launching nothing, when the counters
  *   alone (8 + 4 * num_seqs * num_heads bytes, rounded up to 256) exceed
  *   PA_STATIC_SCRATCH_BYTES.

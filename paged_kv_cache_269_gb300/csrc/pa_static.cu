@@ -16,8 +16,12 @@
 // library holds PA_STATIC_SCRATCH_BYTES of it until the process exits.  In
 // host code its name is only a host-side stand-in, so the device address is
 // looked up with cudaGetSymbolAddress, once per device, on the first call made
-// while that device is current.
+// while that device is current, and cached for the life of the process (a
+// cudaDeviceReset invalidates it, as it does every per-device address the
+// library caches).  Argument checks all run before that look-up, so a call
+// that is rejected launches nothing.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -56,6 +60,8 @@ int scratch_address(unsigned char **out) {
 
 size_t round_up_256(size_t x) { return (x + 255) / 256 * 256; }
 
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 }  // namespace
 }  // namespace pa
 
@@ -66,23 +72,30 @@ extern "C" int pa_decode_static(void *out, const void *q, const void *k_cache,
     using namespace pa;
     const size_t size_error = static_cast<size_t>(-1);
     if (!dims) return PA_ERR_NULL;
+    // Every check that needs no GPU comes first, in pa_decode_ws's order, so
+    // that a rejected call neither touches the device nor queues anything.
     const size_t counters = pa_decode_counters_bytes(dims);
     if (counters == 0) {
         // invalid dims: let the regular checks report the exact reason
         return pa_decode_ws(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                             max_blocks_per_seq, dims, 0, nullptr, 0, nullptr, 0, stream);
     }
+    if (max_blocks_per_seq <= 0) return PA_ERR_SHAPE;
+    size_t partials = pa_decode_workspace_bytes(dims, max_blocks_per_seq, 0);
+    if (partials == size_error) return PA_ERR_SHAPE;
+    if (dims->num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_NULL;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_ALIGN;
+    if (!isfinite(scale)) return PA_ERR_SHAPE;
     const size_t counters_region = round_up_256(counters);
     if (counters_region > kScratchBytes) return PA_ERR_WORKSPACE;  // too many (seq, head) pairs
 
     // Partition length: the library default if its partial results fit next
     // to the counters, else doubled until they fit; a single pass over each
     // context (no partials at all) always fits.
-    if (max_blocks_per_seq <= 0 || dims->block_size <= 0) return PA_ERR_SHAPE;
     const long long single_pass = static_cast<long long>(max_blocks_per_seq) * dims->block_size;
     int32_t partition = 0;
-    size_t partials = pa_decode_workspace_bytes(dims, max_blocks_per_seq, partition);
-    if (partials == size_error) return PA_ERR_SHAPE;
     long long tokens = 512;
     while (counters_region + partials > kScratchBytes) {
         if (tokens >= single_pass || tokens > 0x40000000LL) tokens = single_pass;
@@ -93,7 +106,6 @@ extern "C" int pa_decode_static(void *out, const void *q, const void *k_cache,
         tokens *= 2;
     }
     if (counters_region + partials > kScratchBytes) return PA_ERR_WORKSPACE;
-    if (dims->num_seqs == 0) return PA_OK;
 
     unsigned char *scratch = nullptr;
     int rc = scratch_address(&scratch);

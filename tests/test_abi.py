@@ -90,6 +90,30 @@ def test_decode_rejects_null_and_alignment(lib):
     assert lib.pa_decode(fake, fake, fake, fake, fake, fake, 0.1, 8, None, None) == -1
 
 
+def test_decode_static_rejects_before_touching_the_device(lib):
+    # Every rejection below happens on the host, before the scratch array's
+    # address is looked up or its counters are cleared: no CUDA call is made,
+    # which is why this runs without a GPU.
+    d = _dims()
+    fake = ctypes.c_void_p(0x100000)           # never dereferenced: checks fail first
+
+    def call(out=fake, q=fake, scale=0.1, mb=8, dims=d):
+        return lib.pa_decode_static(out, q, fake, fake, fake, fake, scale, mb,
+                                    ctypes.byref(dims) if dims is not None else None, None)
+
+    assert call(out=None) == -1
+    assert call(q=None) == -1
+    assert call(dims=None) == -1
+    assert call(out=ctypes.c_void_p(0x100002)) == -4
+    assert call(scale=float("nan")) == -2
+    assert call(scale=float("inf")) == -2
+    assert call(mb=0) == -2
+    assert call(dims=_dims(D=96)) == -3
+    assert call(dims=_dims(S=0), out=None) == 0   # an empty batch is a no-op
+    # 70000 x 64 (sequence, head) tickets need more than the 16 MiB array
+    assert call(dims=pa.Dims(70000, 64, 128, 16, 1024)) == -5
+
+
 def test_empty_batches_are_noops(lib):
     d = _dims(S=0)
     assert lib.pa_decode_ws(None, None, None, None, None, None, 0.1, 8, ctypes.byref(d), 0,

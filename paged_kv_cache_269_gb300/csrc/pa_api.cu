@@ -381,6 +381,7 @@ int pa_decode_ws(void *out, const void *q, const void *k_cache, const void *v_ca
     a.group_prefix_blocks = nullptr;
     a.num_groups = 0;
     a.rows_cap = 0;
+    a.chunk_shift = 0;
     cudaError_t e = launch_decode(a, dims->dtype, dims->head_dim, dims->block_size, st->num_sms,
                                   static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidConfiguration) return PA_ERR_UNSUPPORTED;  // too many sequences
@@ -528,6 +529,7 @@ int pa_decode_shared_prefix_ws(void *out, const void *q, const void *k_cache, co
     a.group_prefix_blocks = groups ? group_prefix_blocks : nullptr;
     a.num_groups = groups ? num_groups : 0;
     a.rows_cap = static_cast<int32_t>(pairs * 256 > 0x7fffffffLL ? 0x7fffffffLL : pairs * 256);
+    a.chunk_shift = 0;
     const cudaError_t e = launch_decode(a, dims->dtype, dims->head_dim, dims->block_size,
                                         st->num_sms, s);
     if (e == cudaErrorInvalidConfiguration) return PA_ERR_UNSUPPORTED;  // too many sequences

@@ -34,6 +34,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -121,17 +123,20 @@ struct Cfg {
     // registers so that as many CTAs fit.
     static constexpr int MIN_BLOCKS = clamp_int(228 * 1024 / (OFF_SEQ + 8 * 1024 + 1024), 1, 8);
 
-    // Shared-prefix mode (num_groups >= 0) adds each sequence's first block
-    // and place in the work order, the group starts, the order's length
-    // classes, and the deferred-merge lists (kept small: at S = 128 four
-    // CTAs per SM still fit).
-    __host__ __device__ static size_t seq_ints(int num_seqs, int num_groups) {
+    // Plain mode keeps, per sequence, its partition count (as a prefix) and
+    // context length (chunk_shift 0), or one partition count per chunk of
+    // 2^chunk_shift sequences.  Shared-prefix mode (num_groups >= 0) adds each
+    // sequence's first block and place in the work order, the group starts,
+    // the order's length classes, and the deferred-merge lists (kept small:
+    // at S = 128 four CTAs per SM still fit).
+    __host__ __device__ static size_t seq_ints(int num_seqs, int num_groups, int chunk_shift) {
         const size_t S = static_cast<size_t>(num_seqs);
-        return num_groups < 0 ? 2 * S + 1
-                              : 4 * S + 1 + 2 * static_cast<size_t>(num_groups) + 1 + KEYS;
+        if (num_groups >= 0) return 4 * S + 1 + 2 * static_cast<size_t>(num_groups) + 1 + KEYS;
+        if (chunk_shift == 0) return 2 * S + 1;
+        return ((S + (size_t{1} << chunk_shift) - 1) >> chunk_shift) + 1;
     }
-    static size_t smem_bytes(int num_seqs, int num_groups) {
-        size_t n = static_cast<size_t>(OFF_SEQ) + seq_ints(num_seqs, num_groups) * 4;
+    static size_t smem_bytes(int num_seqs, int num_groups, int chunk_shift) {
+        size_t n = static_cast<size_t>(OFF_SEQ) + seq_ints(num_seqs, num_groups, chunk_shift) * 4;
         if (num_groups >= 0) n = (n + 7) / 8 * 8 + static_cast<size_t>(NC) * DEFER * 8;
         return n;
     }
@@ -433,7 +438,11 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     int *gpre = gstart + G + 1;                                // [G]
     int *classes = gpre + G;                                   // [KEYS]
     uint2 *defer = reinterpret_cast<uint2 *>(
-        smem + (C::OFF_SEQ + C::seq_ints(S, G) * 4 + 7) / 8 * 8);   // [NC][DEFER]
+        smem + (C::OFF_SEQ + C::seq_ints(S, G, 0) * 4 + 7) / 8 * 8);   // [NC][DEFER]
+    // Chunked plain mode: prefix[c] counts the partitions of the sequences
+    // before chunk c (chunks of 2^CS sequences); ctx_of is not kept.
+    const int CS = shared ? 0 : a.chunk_shift;
+    const int nch = CS > 0 ? static_cast<int>((static_cast<long long>(S) + (1 << CS) - 1) >> CS) : 0;
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -481,7 +490,32 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         malformed = __syncthreads_or(bad) != 0;
         if (malformed && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_PREFIX);
     }
-    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    // partitions of a context of c tokens (c within [0, ctx_cap]); an empty
+    // context still takes one unit, which writes its zero output row
+    auto parts_of = [&](int c) {
+        const int nb = (c + B - 1) / B;
+        return nb == 0 ? 1 : (nb + TPU - 1) / TPU;
+    };
+    if (CS > 0) {   // one warp per chunk: its sequences' partition counts, summed
+        const int nwarps = static_cast<int>(blockDim.x / 32);
+        for (int c = warp; c < nch; c += nwarps) {
+            int cnt = 0;
+            for (int i = lane; i < (1 << CS); i += 32) {
+                const int s = (c << CS) + i;
+                if (s >= S) break;
+                int x = a.context_lens[s];
+                if (x < 0 || x > ctx_cap) {
+                    atomicOr(a.err, PA_DEVERR_CONTEXT);
+                    x = x < 0 ? 0 : ctx_cap;
+                }
+                cnt += parts_of(x);
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(kFull, cnt, off);
+            if (lane == 0) prefix[c + 1] = cnt;
+        }
+    }
+    for (int s = threadIdx.x; s < (CS > 0 ? 0 : S); s += blockDim.x) {
         const int c_in = shared ? ctx_of[s] : a.context_lens[s];
         int c = c_in;
         if (c < 0 || c > ctx_cap) {
@@ -556,16 +590,18 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
             __syncwarp();
         }
     }
+    // entries of the prefix: one per sequence, or one per chunk
+    const int NE = CS > 0 ? nch : S;
     if (warp == C::NC) {  // exclusive prefix over the order of partition counts
         int running = 0;
-        for (int base = 0; base < S; base += 32) {
+        for (int base = 0; base < NE; base += 32) {
             const int s = base + lane;
             int v = 0;
-            if (s < S && shared) {   // partitions of the sequence in place s
+            if (s < NE && shared) {   // partitions of the sequence in place s
                 const int r = order[s];
                 const int rest = (ctx_of[r] + B - 1) / B - start_of[r];
                 v = rest == 0 ? 1 : (rest + TPU - 1) / TPU;
-            } else if (s < S) {
+            } else if (s < NE) {
                 v = prefix[s + 1];
             }
 #pragma unroll
@@ -573,14 +609,14 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                 const int y = __shfl_up_sync(kFull, v, off);
                 if (lane >= off) v += y;
             }
-            if (s < S) prefix[s + 1] = running + v;
+            if (s < NE) prefix[s + 1] = running + v;
             running += __shfl_sync(kFull, v, 31);
         }
         if (lane == 0) prefix[0] = 0;
     }
     __syncthreads();
 
-    const uint32_t num_units = static_cast<uint32_t>(prefix[S]) * static_cast<uint32_t>(H);
+    const uint32_t num_units = static_cast<uint32_t>(prefix[NE]) * static_cast<uint32_t>(H);
 
     if (warp == C::NC) {
         // ================= producer warp =================
@@ -595,15 +631,61 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
             if (lane == 0) pending = atomicAdd(&a.counters[0], 1u);  // prefetch the next grab
             const int g = static_cast<int>(u / H);
             const int h = static_cast<int>(u - static_cast<uint32_t>(g) * H);
-            int lo = 0, hi = S - 1;  // position i with prefix[i] <= g < prefix[i + 1]
+            int lo = 0, hi = NE - 1;  // entry i with prefix[i] <= g < prefix[i + 1]
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
             }
-            const int s = shared ? order[lo] : lo;
-            const int p = g - prefix[lo];
-            const int np = prefix[lo + 1] - prefix[lo];
-            const int ctx = ctx_of[s];
+            int s, p, np, ctx;
+            if (CS == 0) {
+                s = shared ? order[lo] : lo;
+                p = g - prefix[lo];
+                np = prefix[lo + 1] - prefix[lo];
+                ctx = ctx_of[s];
+            } else {
+                // chunk lo: each lane takes 2^(CS-5) consecutive sequences,
+                // a warp scan of their partition counts finds the lane whose
+                // range holds partition `rem` of the chunk, and that lane
+                // walks its sequences to the one that holds it
+                const int rem = g - prefix[lo];
+                const int per_lane = 1 << (CS - 5);
+                const int sb = (lo << CS) + lane * per_lane;
+                int tot = 0;
+                for (int i = 0; i < per_lane; ++i) {
+                    if (sb + i >= S) break;
+                    tot += parts_of(min(max(__ldg(a.context_lens + sb + i), 0), ctx_cap));
+                }
+                int inc = tot;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(kFull, inc, off);
+                    if (lane >= off) inc += y;
+                }
+                const unsigned hit = __ballot_sync(kFull, inc > rem);
+                if (hit == 0) {   // only if the lengths changed during the launch
+                    if (lane == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
+                    continue;
+                }
+                const int L = __ffs(hit) - 1;
+                int fs = -1, fp = 0, fnp = 1, fctx = 0;
+                if (lane == L) {
+                    int r = rem - (inc - tot);
+                    for (int i = 0; i < per_lane && sb + i < S; ++i) {
+                        const int c = min(max(__ldg(a.context_lens + sb + i), 0), ctx_cap);
+                        const int n = parts_of(c);
+                        if (r < n) { fs = sb + i; fp = r; fnp = n; fctx = c; break; }
+                        r -= n;
+                    }
+                }
+                s = __shfl_sync(kFull, fs, L);
+                p = __shfl_sync(kFull, fp, L);
+                np = __shfl_sync(kFull, fnp, L);
+                ctx = __shfl_sync(kFull, fctx, L);
+                if (s < 0) {
+                    if (lane == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
+                    continue;
+                }
+            }
             const int nblk = (ctx + B - 1) / B;
             const int first = shared ? start_of[s] : 0;
             bool pre = first > 0;
@@ -913,7 +995,7 @@ struct Variant {
     int dtype, head_dim, block_size;
     const void *kernel;
     int threads;
-    size_t (*smem_bytes)(int, int);
+    size_t (*smem_bytes)(int, int, int);
 };
 
 template <typename E, int D, int B>
@@ -958,6 +1040,58 @@ const Variant *find_variant(int dtype, int head_dim, int block_size) {
 constexpr int kMaxDevices = 64;
 int g_max_dynamic_smem[kMaxDevices] = {0};
 
+// Launch shape of one plain-mode decode: the sequence-state layout, its
+// shared memory and the CTAs per SM it allows.  The last shape computed per
+// device and variant is kept, so repeated calls with the same batch size
+// query the occupancy calculator once.
+struct Shape {
+    int num_seqs = -1, chunk_shift = 0, per_sm = 0;
+    size_t smem = 0;
+};
+Shape g_last_shape[kMaxDevices][kNumVariants];
+std::mutex g_shape_mutex;
+
+cudaError_t occupancy(const Variant *v, size_t smem, int *per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, v->kernel, v->threads, smem);
+}
+
+// Per-sequence state (chunk_shift 0) while it leaves the CTAs per SM at what
+// the fixed footprint alone allows; otherwise the smallest chunk of 2^c
+// sequences (c >= 5) that does, or one chunk for the whole batch.
+cudaError_t plain_shape(const Variant *v, int device, int num_seqs, Shape *out) {
+    const int vi = static_cast<int>(v - variants());
+    {
+        std::lock_guard<std::mutex> lock(g_shape_mutex);
+        const Shape &c = g_last_shape[device][vi];
+        if (c.num_seqs == num_seqs) {
+            *out = c;
+            return cudaSuccess;
+        }
+    }
+    int best = 0;
+    cudaError_t e = occupancy(v, v->smem_bytes(1, -1, 30), &best);
+    if (e != cudaSuccess) return e;
+    Shape sh;
+    sh.num_seqs = num_seqs;
+    for (int cs = 0;; cs = cs == 0 ? 5 : cs + 1) {
+        sh.chunk_shift = cs;
+        sh.smem = v->smem_bytes(num_seqs, -1, cs);
+        const bool one_chunk = cs >= 30 || (cs > 0 && (num_seqs >> cs) == 0);
+        if (sh.smem > static_cast<size_t>(g_max_dynamic_smem[device])) {
+            if (one_chunk) return cudaErrorInvalidConfiguration;
+            continue;
+        }
+        e = occupancy(v, sh.smem, &sh.per_sm);
+        if (e != cudaSuccess) return e;
+        if (sh.per_sm >= best || one_chunk) break;
+    }
+    if (sh.per_sm < 1) return cudaErrorInvalidConfiguration;
+    std::lock_guard<std::mutex> lock(g_shape_mutex);
+    g_last_shape[device][vi] = sh;
+    *out = sh;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 bool decode_variant_supported(int dtype, int head_dim, int block_size) {
@@ -983,7 +1117,8 @@ bool decode_fits(int dtype, int head_dim, int block_size, int num_seqs, int num_
     int device = 0;
     if (!v || cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
         return false;
-    return v->smem_bytes(num_seqs, num_groups) <=
+    if (num_groups < 0) return true;   // plain mode always has a fitting layout
+    return v->smem_bytes(num_seqs, num_groups, 0) <=
            static_cast<size_t>(g_max_dynamic_smem[device]);
 }
 
@@ -995,19 +1130,31 @@ cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int b
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
     if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-    const size_t smem =
-        v->smem_bytes(args.num_seqs, args.group_start != nullptr ? args.num_groups : -1);
-    if (smem > static_cast<size_t>(g_max_dynamic_smem[device])) return cudaErrorInvalidConfiguration;
+    DecodeArgs la = args;
+    size_t smem = 0;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v->kernel, v->threads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (args.group_start != nullptr) {
+        la.chunk_shift = 0;
+        smem = v->smem_bytes(args.num_seqs, args.num_groups, 0);
+        if (smem > static_cast<size_t>(g_max_dynamic_smem[device]))
+            return cudaErrorInvalidConfiguration;
+        e = occupancy(v, smem, &per_sm);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    } else {
+        Shape sh;
+        e = plain_shape(v, device, args.num_seqs, &sh);
+        if (e != cudaSuccess) return e;
+        la.chunk_shift = sh.chunk_shift;
+        smem = sh.smem;
+        per_sm = sh.per_sm;
+    }
     // Persistent grid; never more CTAs than the most work units there can be.
     const long long max_units = static_cast<long long>(args.num_seqs) * args.num_heads * args.max_parts;
     long long grid = static_cast<long long>(per_sm) * num_sms;
     if (grid > max_units) grid = max_units;
     if (grid < 1) grid = 1;
-    void *params[] = {const_cast<DecodeArgs *>(&args)};
+    void *params[] = {&la};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -38,6 +38,12 @@ struct DecodeArgs {
     const int32_t *group_prefix_blocks;  // [num_groups]
     int32_t num_groups;
     int32_t rows_cap;                    // rows per group the prefix kernel computes
+    // Set by launch_decode (plain mode only).  0: every CTA keeps each
+    // sequence's partition count and context length in shared memory.  c > 0:
+    // it keeps one partition count per chunk of 2^c sequences (c >= 5), and
+    // the producer warp resolves a unit's sequence from one coalesced load of
+    // its chunk's context lengths, so large batches keep the CTAs per SM.
+    int32_t chunk_shift;
 };
 
 // Sizes of the two caller buffers of pa_decode_ws.

@@ -134,6 +134,19 @@ def test_many_sequences(dev):
     assert_parity(got, oracle.decode_case(case), "3000 sequences")
 
 
+@pytest.mark.parametrize("n,maxlen,partition_tokens", [(60000, 30, 16), (200000, 20, 0)])
+def test_very_large_batches(dev, n, maxlen, partition_tokens):
+    # Far more sequences than fit one shared-memory entry each: the CTAs keep
+    # one partition count per chunk of 64 (60000) or of 256 and more (200000)
+    # sequences, so each lane of the producer warp resolves several
+    # sequences; 16-token partitions give most sequences several partitions.
+    rng = np.random.default_rng(5)
+    case = _ragged(f"huge{n}", rng.integers(0, maxlen, size=n), H=1, D=64)
+    got, flags, _ = run_gpu(case, dev, partition_tokens)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), f"{n} sequences, P={partition_tokens}")
+
+
 def test_empty_batch(dev):
     import torch
     import paged_kv_cache_269_gb300 as pa
@@ -211,7 +224,8 @@ def test_bad_slot_is_reported(dev):
 # the five workloads at full size, in the launch configuration the bench uses
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("kind", ["tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx"])
+@pytest.mark.parametrize("kind", ["tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx",
+                                  "cb_mix_1k", "cb_mix_4k"])
 def test_workload_full_size(dev, kind):
     case = workloads.make_workload(kind)
     got, flags, d = run_gpu(case, dev)

@@ -428,7 +428,8 @@ def duplicate_prefix(case: DecodeCase) -> DecodeCase:
 # the five named workloads
 # ----------------------------------------------------------------------------
 
-WORKLOADS = ("tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx")
+WORKLOADS = ("tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx", "cb_mix_1k",
+             "cb_mix_4k")
 
 
 def make_workload(kind: str, seed: Optional[int] = None, **kw) -> DecodeCase:
@@ -446,8 +447,13 @@ def make_workload(kind: str, seed: Optional[int] = None, **kw) -> DecodeCase:
                   32 physical blocks (a 512-token system prompt) followed by a
                   private suffix of U[16, 512] tokens.
     long_ctx      8 seqs, 32 heads, D 128, 32768 tokens each (2048 blocks).
+    cb_mix_1k     cb_mix's length recipe at a serving batch of 1024 sequences
+                  (32 heads, D 128; 7.8 GB of K/V).
+    cb_mix_4k     the same recipe at 4096 sequences, with 8 heads of D 128 (the
+                  K/V of a layer with 8 key/value heads; 7.8 GB of K/V).
     """
-    seeds = {"tiny": 1, "llama7b_b64": 2, "cb_mix": 3, "shared_prefix": 4, "long_ctx": 5}
+    seeds = {"tiny": 1, "llama7b_b64": 2, "cb_mix": 3, "shared_prefix": 4, "long_ctx": 5,
+             "cb_mix_1k": 6, "cb_mix_4k": 7}
     if kind not in seeds:
         raise KeyError(kind)
     seed = seeds[kind] if seed is None else seed
@@ -465,6 +471,12 @@ def make_workload(kind: str, seed: Optional[int] = None, **kw) -> DecodeCase:
         prompt = rng.integers(16, 512, size=256, endpoint=True)
         gen = np.minimum(rng.geometric(1.0 / 200.0, size=256), 1000)
         return build_case(kind, prompt + gen, num_heads=32, head_dim=128, seed=seed,
+                          max_blocks_per_seq=blocks_needed(512 + 1000), **kw)
+    if kind in ("cb_mix_1k", "cb_mix_4k"):
+        n, heads = (1024, 32) if kind == "cb_mix_1k" else (4096, 8)
+        prompt = rng.integers(16, 512, size=n, endpoint=True)
+        gen = np.minimum(rng.geometric(1.0 / 200.0, size=n), 1000)
+        return build_case(kind, prompt + gen, num_heads=heads, head_dim=128, seed=seed,
                           max_blocks_per_seq=blocks_needed(512 + 1000), **kw)
     if kind == "shared_prefix":
         suffix = rng.integers(16, 512, size=128, endpoint=True)

@@ -75,12 +75,13 @@ constexpr int kPvWarp0 = 11;        // issues query tile 0's P V products; warp 
 // Register split: launched at 128 per thread (512 threads), the two
 // producer warpgroups (warps 8-15) give registers up to the two softmax
 // warpgroups; the four shares must fit the block's launch allotment of
-// 4 x 128 per lane.
+// 4 x 128 per lane.  At 56 the producer roles compile without spills (at 48
+// the TMA and MMA loops spilled a few words).
 #ifndef PA_PREFILL_REGS_SOFTMAX
-#define PA_PREFILL_REGS_SOFTMAX 208
+#define PA_PREFILL_REGS_SOFTMAX 200
 #endif
 #ifndef PA_PREFILL_REGS_OTHER
-#define PA_PREFILL_REGS_OTHER 48
+#define PA_PREFILL_REGS_OTHER 56
 #endif
 constexpr int kRegsSoftmax = PA_PREFILL_REGS_SOFTMAX;
 constexpr int kRegsOther = PA_PREFILL_REGS_OTHER;

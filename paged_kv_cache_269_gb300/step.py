@@ -17,6 +17,12 @@ also hands over the groups of adjacent rows that share prompt blocks (e.g.
 KVManager.prefix_groups of the batch), staged with the other inputs; unused
 group slots are empty, so the shapes still never change.
 
+PipelinedDecodeStep runs two such steps in turn, each with its own staging
+buffers, so that step k + 1's host-to-device copy (on a copy stream) overlaps
+step k's kernels and the host reads step k's output after step k + 1 has been
+launched.  The kernels of successive steps still run in order on one stream:
+each step's reshape_and_cache writes the cache the next step's decode reads.
+
 This module only orchestrates calls into libpa; all arithmetic runs in its
 kernels.
 """
@@ -31,7 +37,12 @@ from . import (copy_blocks, decode, decode_counters_bytes, decode_shared_prefix,
 
 class DecodeStep:
     def __init__(self, k_cache, v_cache, max_seqs, max_blocks_per_seq, scale, use_graph=True,
-                 partition_tokens=0, stream=None, host_out=False, max_groups=0):
+                 partition_tokens=0, stream=None, host_out=False, max_groups=0,
+                 upload_stream=None):
+        """upload_stream: None keeps the host-to-device copy in the step (in
+        its graph); a stream moves it there, ordered by events: the copy waits
+        until this step's previous kernels stopped reading the device buffer,
+        and the kernels wait for the copy."""
         import torch
         self.torch = torch
         self.k_cache, self.v_cache = k_cache, v_cache
@@ -41,6 +52,10 @@ class DecodeStep:
         self.dev = k_cache.device
         self.dtype = k_cache.dtype
         self.stream = stream or torch.cuda.Stream(self.dev)
+        self.upload_stream = upload_stream
+        self.upload_done = torch.cuda.Event() if upload_stream is not None else None
+        self.compute_done = torch.cuda.Event() if upload_stream is not None else None
+        self.launched = False
         self.use_graph = use_graph
         self.graph = None
         self.G = int(max_groups)
@@ -93,9 +108,12 @@ class DecodeStep:
         """Stage one step's inputs (numpy; n <= max_seqs rows) into the pinned
         buffer; rows n .. max_seqs-1 become padding.  groups (with
         max_groups > 0): (group_start [G + 1], group_prefix_blocks [G]) over
-        the n rows, G <= max_groups; None shares nothing.  Waits for the
-        previous step first, whose copy reads the same pinned buffer."""
-        self.stream.synchronize()
+        the n rows, G <= max_groups; None shares nothing.  Waits first for
+        the previous copy out of the same pinned buffer (the previous step)."""
+        if self.upload_stream is None:
+            self.stream.synchronize()
+        elif self.launched:
+            self.upload_done.synchronize()
         n = len(lens)
         if n > self.S:
             raise ValueError("more sequences than max_seqs")
@@ -122,7 +140,8 @@ class DecodeStep:
 
     def _body(self):
         d = self.d
-        self.devbuf.copy_(self.host, non_blocking=True)
+        if self.upload_stream is None:
+            self.devbuf.copy_(self.host, non_blocking=True)
         reshape_and_cache(d["k_new"], d["v_new"], self.k_cache, self.v_cache, d["slots"])
         if self.G > 0:
             decode_shared_prefix(self.dst, d["q"], self.k_cache, self.v_cache, d["tables"],
@@ -142,14 +161,30 @@ class DecodeStep:
                                          device=self.dev)
                 copy_blocks(self.k_cache, self.v_cache, self.k_cache, self.v_cache, t)
 
+    def _upload(self):
+        """With an upload stream: copy the staged inputs there once this
+        step's previous kernels are done with the device buffer, and make the
+        step's stream wait for the copy."""
+        torch = self.torch
+        if self.upload_stream is None:
+            return
+        with torch.cuda.stream(self.upload_stream):
+            if self.launched:
+                self.upload_stream.wait_event(self.compute_done)
+            self.devbuf.copy_(self.host, non_blocking=True)
+            self.upload_done.record(self.upload_stream)
+        self.stream.wait_event(self.upload_done)
+
     def launch(self):
         """Enqueue the staged step on self.stream; returns the output tensor
         (valid once the stream reaches this point) -- the pinned host copy
         when the step was built with host_out."""
         torch = self.torch
+        self._upload()
         if not self.use_graph:
             with torch.cuda.stream(self.stream):
                 self._body()
+            self._done()
             return self.out if self.out_host is None else self.out_host
         if self.graph is None:
             with torch.cuda.stream(self.stream):
@@ -160,4 +195,70 @@ class DecodeStep:
                 self._body()
         with torch.cuda.stream(self.stream):
             self.graph.replay()
+        self._done()
         return self.out if self.out_host is None else self.out_host
+
+    def _done(self):
+        self.launched = True
+        if self.compute_done is not None:
+            self.compute_done.record(self.stream)
+
+    def synchronize(self):
+        """Wait until this step's last launch has finished (its output is then
+        readable)."""
+        if self.compute_done is not None and self.launched:
+            self.compute_done.synchronize()
+        else:
+            self.stream.synchronize()
+
+
+class PipelinedDecodeStep:
+    """Two DecodeSteps used in turn: step k + 1's inputs are copied to the
+    device on a copy stream while step k's kernels run, and step k's output
+    is read after step k + 1 has been launched.
+
+    submit(...) stages one step's inputs (as DecodeStep.prepare) into the next
+    slot and launches it, returning a ticket; result(ticket) waits for that
+    step and returns its output (a pinned host tensor with host_out).  The
+    output buffer of a slot is rewritten by the step submitted two tickets
+    later, so read a result before submitting the step after next.
+    prepare() / launch() split submit for callers that relaunch staged
+    inputs."""
+
+    def __init__(self, k_cache, v_cache, max_seqs, max_blocks_per_seq, scale, use_graph=True,
+                 partition_tokens=0, stream=None, host_out=False, max_groups=0, depth=2):
+        import torch
+        self.stream = stream or torch.cuda.Stream(k_cache.device)
+        self.upload_stream = torch.cuda.Stream(k_cache.device)
+        self.steps = [DecodeStep(k_cache, v_cache, max_seqs, max_blocks_per_seq, scale,
+                                 use_graph=use_graph, partition_tokens=partition_tokens,
+                                 stream=self.stream, host_out=host_out, max_groups=max_groups,
+                                 upload_stream=self.upload_stream) for _ in range(depth)]
+        self.next = 0
+
+    def prepare(self, *args, **kw):
+        """Stage inputs into the slot the next launch() uses."""
+        self.steps[self.next % len(self.steps)].prepare(*args, **kw)
+
+    def launch(self):
+        """Launch the next slot's staged inputs; returns its ticket."""
+        t = self.next
+        self.steps[t % len(self.steps)].launch()
+        self.next += 1
+        return t
+
+    def submit(self, *args, **kw):
+        self.prepare(*args, **kw)
+        return self.launch()
+
+    def result(self, ticket):
+        if not self.next - len(self.steps) <= ticket < self.next:
+            raise ValueError("not one of the last steps submitted (a later step has "
+                             "rewritten its output, or it was never submitted)")
+        st = self.steps[ticket % len(self.steps)]
+        st.synchronize()
+        return st.out if st.out_host is None else st.out_host
+
+    def copy_on_write(self, pairs):
+        """Make copy-on-write copies before the next step (on the step stream)."""
+        self.steps[0].copy_on_write(pairs)

@@ -7,7 +7,9 @@ and decodes.  After every step the output is compared with the oracle run on a
 host mirror of the cache that receives the same copies and writes.  The loop
 runs eagerly and replayed from a CUDA graph, with plain decode and with the
 shared-prefix decode (the batch ordered so that sharers are adjacent, the
-groups taken from the manager's sharing records every step)."""
+groups taken from the manager's sharing records every step), and pipelined:
+two staging slots in turn, each step's upload on a copy stream overlapping the
+previous step, and each step's output read after the next one is submitted."""
 import numpy as np
 import pytest
 
@@ -37,13 +39,15 @@ def _normal(rng, shape):
     return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
 
 
-@pytest.mark.parametrize("use_graph,host_out,shared", [(False, False, False), (True, False, False),
-                                                       (True, True, False), (False, False, True),
-                                                       (True, False, True)])
-def test_continuous_batching_loop(dev, use_graph, host_out, shared):
+@pytest.mark.parametrize("use_graph,host_out,shared,pipelined",
+                         [(False, False, False, False), (True, False, False, False),
+                          (True, True, False, False), (False, False, True, False),
+                          (True, False, True, False), (True, True, False, True),
+                          (False, False, True, True)])
+def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined):
     import torch
     import paged_kv_cache_269_gb300 as pa
-    from paged_kv_cache_269_gb300.step import DecodeStep
+    from paged_kv_cache_269_gb300.step import DecodeStep, PipelinedDecodeStep
     rng = np.random.default_rng(77 + use_graph)
     mgr = pa.KVManager(N, B, MB, shuffle_seed=5)
     mirror_k = np.full((N, H, B, D), np.nan, np.float16)
@@ -51,8 +55,20 @@ def test_continuous_batching_loop(dev, use_graph, host_out, shared):
     kc = torch.from_numpy(mirror_k).to(dev)
     vc = torch.from_numpy(mirror_v).to(dev)
     scale = float(np.float32(1 / np.sqrt(D)))
-    step = DecodeStep(kc, vc, SMAX, MB, scale, use_graph=use_graph, partition_tokens=64,
-                      host_out=host_out, max_groups=SMAX if shared else 0)
+    # pipelined: two staging slots, step k + 1's upload overlapping step k,
+    # each output checked after the next step has been submitted
+    kind = PipelinedDecodeStep if pipelined else DecodeStep
+    step = kind(kc, vc, SMAX, MB, scale, use_graph=use_graph, partition_tokens=64,
+                host_out=host_out, max_groups=SMAX if shared else 0)
+    pending = []   # (ticket, n, reference, label) of submitted steps not yet checked
+
+    def check(ticket, n, ref, label):
+        out = step.result(ticket) if pipelined else step.launched_out
+        if not pipelined:
+            step.stream.synchronize()
+        assert out.is_cuda != host_out              # the pinned host copy with host_out
+        assert_parity(out[:n].cpu().numpy(), ref, label)
+        assert (out[n:].cpu().numpy() == 0).all()          # padding rows
     grouped_steps = 0
 
     def write(slots, k, v):
@@ -117,15 +133,21 @@ def test_continuous_batching_loop(dev, use_graph, host_out, shared):
         if shared and (groups[1] > 0).any():
             grouped_steps += 1
         step.prepare(q, kn, vn, np.asarray(slots, np.int32), tables, lens, groups=groups)
-        out = step.launch()
-        step.stream.synchronize()
-        assert out.is_cuda != host_out              # the pinned host copy with host_out
-        got = out[:n].cpu().numpy()
+        if pipelined:
+            ticket = step.launch()
+        else:
+            step.launched_out = step.launch()
+            ticket = it
         mirror_k, mirror_v = oracle.reshape_and_cache(kn, vn, mirror_k, mirror_v,
                                                       np.asarray(slots, np.int32))
         ref = oracle.decode(q, mirror_k, mirror_v, tables, lens, scale)
-        assert_parity(got, ref, f"step {it} (graph={use_graph}, shared={shared})")
-        assert (out[n:].cpu().numpy() == 0).all()          # padding rows
+        pending.append((ticket, n, ref, f"step {it} (graph={use_graph}, shared={shared}, "
+                                        f"pipelined={pipelined})"))
+        # a pipelined step's output is read once the next step is in flight
+        while len(pending) > (1 if pipelined else 0):
+            check(*pending.pop(0))
+    while pending:
+        check(*pending.pop(0))
     assert pa.device_errors(stream=step.stream) == 0
     if shared:
         assert grouped_steps >= 20                         # the prefix path was exercised

@@ -474,8 +474,8 @@ int pa_decode_shared_prefix_ws(void *out, const void *q, const void *k_cache, co
     rc = current_device_state(&st);
     if (rc != PA_OK) return rc;
     // checked before the prefix kernel writes anything into the counters
-    if (!decode_fits(dims->dtype, dims->head_dim, dims->block_size, dims->num_seqs,
-                     groups ? num_groups : -1))
+    if (!decode_fits(dims->dtype, dims->head_dim, dims->block_size, dims->num_heads,
+                     dims->num_seqs, groups ? num_groups : -1))
         return PA_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);

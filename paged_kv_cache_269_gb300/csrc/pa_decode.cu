@@ -69,19 +69,53 @@ constexpr int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? 
 #define PA_DECODE_DESC_SLOTS 2
 #endif
 
-template <int D, int B>
+// Heads per work unit by tile size (B x D x 2 bytes), overridable at build
+// time.  In the [N, H, B, D] layout the tiles of heads h .. h + HG - 1 of one
+// block are one contiguous run, so a unit of HG heads moves each block's K
+// (and V) with one bulk copy of HG tiles and reads its table slice once.
+// Measured on a LLaMA-shaped batch (H x D = 4096), fraction of the copy rate
+// with one head per unit -> the group below: 1 KiB tiles (D 64 x B 8) 0.835
+// -> 0.885 with 4 heads; 2 KiB (D 64 x B 16, D 128 x B 8) 0.930 -> 0.975 and
+// 0.937 -> 0.960 with 2; 4 KiB tiles of D 64 x B 32 and D 256 x B 8 0.968 ->
+// 0.981 and 0.960 -> 0.970 with 2, while D 128 x B 16 lost 0.6 % with 2 and
+// keeps one head per unit.
+#ifndef PA_DECODE_HG_1K
+#define PA_DECODE_HG_1K 4
+#endif
+#ifndef PA_DECODE_HG_2K
+#define PA_DECODE_HG_2K 2
+#endif
+#ifndef PA_DECODE_HG_4K
+#define PA_DECODE_HG_4K 2
+#endif
+#ifndef PA_DECODE_HG_D128_B16
+#define PA_DECODE_HG_D128_B16 1
+#endif
+
+__host__ __device__ constexpr int preferred_heads(int head_dim, int block_size) {
+    return (head_dim == 128 && block_size == 16) ? PA_DECODE_HG_D128_B16
+           : block_size * head_dim * 2 <= 1024 ? PA_DECODE_HG_1K
+           : block_size * head_dim * 2 <= 2048 ? PA_DECODE_HG_2K
+           : block_size * head_dim * 2 <= 4096 ? PA_DECODE_HG_4K : 1;
+}
+
+template <int D, int B, int HG = 1>
 struct Cfg {
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
     static_assert(B == 8 || B == 16 || B == 32, "block_size");
+    static_assert(HG == 1 || HG == 2 || HG == 4, "heads per unit");
     static constexpr int NC = PA_DECODE_CONSUMER_WARPS;  // consumer warps
+    static_assert(NC % HG == 0, "each head of a unit gets the same number of warps");
     static constexpr int THREADS = (NC + 1) * 32;     // + one producer warp
     static constexpr int TILE_BYTES = B * D * 2;      // one K (or V) tile, fp16
-    // Blocks per ring stage: tiles under 2 KiB (D 64 x B 8) are grouped four to
-    // a stage, so that one barrier, tag and hand-off carries 4 KiB of K and of
-    // V; every other shape keeps one block per stage.
-    static constexpr int R = TILE_BYTES < 2048 ? 4096 / TILE_BYTES : 1;
+    // Blocks per ring stage: with one head per unit, tiles under 2 KiB (D 64 x
+    // B 8) are grouped four blocks to a stage, so that one barrier, tag and
+    // hand-off carries 4 KiB of K and of V; every other shape, and every unit
+    // of several heads, keeps one block per stage.
+    static constexpr int R = (HG == 1 && TILE_BYTES < 2048) ? 4096 / TILE_BYTES : 1;
     static_assert(32 % R == 0, "a stage never straddles a 32-entry table slice");
-    static constexpr int STAGE_BYTES = 2 * R * TILE_BYTES;  // [K tiles][V tiles]
+    // [K: R blocks x HG heads][V: the same]
+    static constexpr int STAGE_BYTES = 2 * R * HG * TILE_BYTES;
     static constexpr int STAGE_BUDGET = PA_DECODE_STAGE_KIB * 1024;
     // At least 4 stages, unless a 4-stage ring of very large tiles would
     // exceed twice the budget (D 256 x B 32: 128 KiB, one CTA per SM); then
@@ -104,7 +138,7 @@ struct Cfg {
 
     static constexpr int OFF_STAGES = 0;
     static constexpr int OFF_DESC_Q = NS * STAGE_BYTES;
-    static constexpr int OFF_MERGE_ACC = OFF_DESC_Q + ND * D * 2;
+    static constexpr int OFF_MERGE_ACC = OFF_DESC_Q + ND * HG * D * 2;
     static constexpr int OFF_MERGE_ML = OFF_MERGE_ACC + ND * NC * D * 4;
     static constexpr int OFF_PROBS = OFF_MERGE_ML + ND * NC * 8;
     static constexpr int OFF_META = OFF_PROBS + NC * B * 4;
@@ -400,10 +434,10 @@ __device__ __forceinline__ void combine_partials(const DecodeArgs &a, size_t sh,
     store_out<E, DPL>(a.out + sh * D + lane * DPL, go, GL > 0.f ? 1.f / GL : 0.f);
 }
 
-template <typename E, int D, int B>
-__global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
+template <typename E, int D, int B, int HG>
+__global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLOCKS)
     decode_kernel(const DecodeArgs a) {
-    using C = Cfg<D, B>;
+    using C = Cfg<D, B, HG>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BARS);
     uint64_t *empty = full + C::NS;
@@ -452,7 +486,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], HG);   // one arrival per warp reading the stage
             stage_tag[i] = 0xffffffffu;
         }
         for (int i = 0; i < C::ND; ++i) {
@@ -616,7 +650,9 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
     }
     __syncthreads();
 
-    const uint32_t num_units = static_cast<uint32_t>(prefix[NE]) * static_cast<uint32_t>(H);
+    // units: (entry of the order, partition, group of HG heads), heads fastest
+    const int HGR = H / HG;   // head groups (the host launches HG > 1 only if HG divides H)
+    const uint32_t num_units = static_cast<uint32_t>(prefix[NE]) * static_cast<uint32_t>(HGR);
 
     if (warp == C::NC) {
         // ================= producer warp =================
@@ -629,8 +665,8 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
             const uint32_t u = __shfl_sync(kFull, pending, 0);
             if (u >= num_units) break;
             if (lane == 0) pending = atomicAdd(&a.counters[0], 1u);  // prefetch the next grab
-            const int g = static_cast<int>(u / H);
-            const int h = static_cast<int>(u - static_cast<uint32_t>(g) * H);
+            const int g = static_cast<int>(u / HGR);
+            const int h = static_cast<int>(u - static_cast<uint32_t>(g) * HGR) * HG;   // first head
             int lo = 0, hi = NE - 1;  // entry i with prefix[i] <= g < prefix[i + 1]
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -719,9 +755,10 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                 int *m = meta + slot * C::META_INTS;
                 m[0] = s; m[1] = h; m[2] = p; m[3] = nt; m[4] = ctx; m[5] = np;
                 m[6] = t0; m[7] = pre ? 1 : 0;
-                mbar_arrive_expect_tx(&desc_full[slot], D * 2);
-                bulk_copy_g2s(desc_q + slot * D, a.q + (static_cast<size_t>(s) * H + h) * D, D * 2,
-                              &desc_full[slot]);
+                // the queries of heads h .. h + HG - 1: one contiguous run
+                mbar_arrive_expect_tx(&desc_full[slot], HG * D * 2);
+                bulk_copy_g2s(desc_q + slot * HG * D, a.q + (static_cast<size_t>(s) * H + h) * D,
+                              HG * D * 2, &desc_full[slot]);
             }
             ++dq;
 
@@ -740,11 +777,13 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                             stage_ok[st] = in_pool ? 1 : 0;
                             stage_tag[st] = kq;
                             if (in_pool) {
+                                // heads h .. h + HG - 1 of the block: HG adjacent tiles
                                 const size_t off = (static_cast<size_t>(phys) * H + h) * (B * D);
                                 uint8_t *dst = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
-                                mbar_arrive_expect_tx(&full[st], 2 * C::TILE_BYTES);
-                                bulk_copy_g2s(dst, a.k_cache + off, C::TILE_BYTES, &full[st]);
-                                bulk_copy_g2s(dst + C::TILE_BYTES, a.v_cache + off, C::TILE_BYTES, &full[st]);
+                                mbar_arrive_expect_tx(&full[st], 2 * HG * C::TILE_BYTES);
+                                bulk_copy_g2s(dst, a.k_cache + off, HG * C::TILE_BYTES, &full[st]);
+                                bulk_copy_g2s(dst + HG * C::TILE_BYTES, a.v_cache + off,
+                                              HG * C::TILE_BYTES, &full[st]);
                             } else {
                                 atomicOr(a.err, PA_DEVERR_TABLE);
                                 mbar_arrive(&full[st]);
@@ -844,13 +883,16 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         const int *m = meta + slot * C::META_INTS;
         const int s = m[0];
         if (s < 0) break;
-        const int h = m[1], p = m[2], nt = m[3], ctx = m[4], np = m[5], t0 = m[6];
+        // this warp's head: gw-th of the unit's HG heads; its blocks are
+        // every (NC / HG)-th one from w / HG
+        const int gw = w % HG;
+        const int h = m[1] + gw, p = m[2], nt = m[3], ctx = m[4], np = m[5], t0 = m[6];
         // with a shared prefix, slot 0 of (s, h) holds the prefix kernel's partial
         const int pre = m[7];
 
         float qf[8];
-        const uint4 qraw =
-            *reinterpret_cast<const uint4 *>(desc_q + slot * D + (lane % C::LPT) * 8);
+        const uint4 qraw = *reinterpret_cast<const uint4 *>(desc_q + (slot * HG + gw) * D +
+                                                            (lane % C::LPT) * 8);
         {
             const float2 q0 = E::pair(qraw.x), q1 = E::pair(qraw.y), q2 = E::pair(qraw.z),
                          q3 = E::pair(qraw.w);
@@ -863,7 +905,7 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         for (int i = 0; i < C::DPL; ++i) acc[i] = 0.f;
 
         if constexpr (C::R == 1) {
-            for (int j = w; j < nt; j += C::NC) {
+            for (int j = w / HG; j < nt; j += C::NC / HG) {
                 const uint32_t k = kq + j;
                 const int st = static_cast<int>(k % C::NS);
                 w_ok = wait_value(&stage_tag[st], k, abort_flag, a.err) &&
@@ -872,9 +914,10 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
                 if (stage_ok[st]) {
                     const int tok0 = (t0 + j) * B;
                     const int nvalid = min(B, ctx - tok0);
-                    const uint8_t *ktile = smem + C::OFF_STAGES + st * C::STAGE_BYTES;
-                    consume_tile<E, D, B>(ktile, ktile + C::TILE_BYTES, qraw, qf, a.scale_log2,
-                                          nvalid, run_max, run_sum, acc, probs, lane);
+                    const uint8_t *ktile =
+                        smem + C::OFF_STAGES + st * C::STAGE_BYTES + gw * C::TILE_BYTES;
+                    consume_tile<E, D, B>(ktile, ktile + HG * C::TILE_BYTES, qraw, qf,
+                                          a.scale_log2, nvalid, run_max, run_sum, acc, probs, lane);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
@@ -911,19 +954,23 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
         __syncwarp();
         if (lane == 0) mbar_arrive(&merge_full[slot]);
 
-        const int owner = static_cast<int>(dq % C::NC);
-        if (w == owner) {
+        // one owner per head of the unit: it merges the NC / HG warps that
+        // read that head (warps gw, gw + HG, ...), rotating with the unit
+        constexpr int WPH = C::NC / HG;   // warps per head
+        const int owner_rank = static_cast<int>(dq % WPH);
+        if (w / HG == owner_rank) {
             w_ok = mbar_wait(&merge_full[slot], (dq / C::ND) & 1u, abort_flag, a.err);
             if (!__all_sync(kFull, w_ok)) return;
             float M = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < C::NC; ++i) M = fmaxf(M, merge_ml[slot * C::NC + i].x);
+            for (int k = 0; k < WPH; ++k) M = fmaxf(M, merge_ml[slot * C::NC + k * HG + gw].x);
             float L = 0.f;
             float o[C::DPL];
 #pragma unroll
             for (int i = 0; i < C::DPL; ++i) o[i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < C::NC; ++i) {
+            for (int k = 0; k < WPH; ++k) {
+                const int i = k * HG + gw;
                 const float2 ml = merge_ml[slot * C::NC + i];
                 if (ml.x == -INFINITY) continue;  // a warp with no tile of this unit
                 const float f = exp2f(ml.x - M);
@@ -992,46 +1039,54 @@ __global__ void __launch_bounds__(Cfg<D, B>::THREADS, Cfg<D, B>::MIN_BLOCKS)
 }
 
 struct Variant {
-    int dtype, head_dim, block_size;
+    int dtype, head_dim, block_size, hg;
     const void *kernel;
     int threads;
     size_t (*smem_bytes)(int, int, int);
 };
 
-template <typename E, int D, int B>
+template <typename E, int D, int B, int HG>
 Variant make_variant() {
-    return Variant{E::kBf16 ? PA_DTYPE_BF16 : PA_DTYPE_F16, D, B,
-                   reinterpret_cast<const void *>(&decode_kernel<E, D, B>), Cfg<D, B>::THREADS,
-                   &Cfg<D, B>::smem_bytes};
+    return Variant{E::kBf16 ? PA_DTYPE_BF16 : PA_DTYPE_F16, D, B, HG,
+                   reinterpret_cast<const void *>(&decode_kernel<E, D, B, HG>),
+                   Cfg<D, B, HG>::THREADS, &Cfg<D, B, HG>::smem_bytes};
+}
+
+// Two kernels per shape: one head per unit, and the preferred head group
+// (the same kernel again when that is one head).
+template <typename E, int D, int B>
+void add_shape(Variant *v) {
+    v[0] = make_variant<E, D, B, 1>();
+    v[1] = make_variant<E, D, B, preferred_heads(D, B)>();
 }
 
 template <typename E>
 void add_variants(Variant *v) {
-    v[0] = make_variant<E, 64, 8>();   v[1] = make_variant<E, 64, 16>();
-    v[2] = make_variant<E, 64, 32>();  v[3] = make_variant<E, 128, 8>();
-    v[4] = make_variant<E, 128, 16>(); v[5] = make_variant<E, 128, 32>();
-    v[6] = make_variant<E, 256, 8>();  v[7] = make_variant<E, 256, 16>();
-    v[8] = make_variant<E, 256, 32>();
+    add_shape<E, 64, 8>(v + 0);   add_shape<E, 64, 16>(v + 2);   add_shape<E, 64, 32>(v + 4);
+    add_shape<E, 128, 8>(v + 6);  add_shape<E, 128, 16>(v + 8);  add_shape<E, 128, 32>(v + 10);
+    add_shape<E, 256, 8>(v + 12); add_shape<E, 256, 16>(v + 14); add_shape<E, 256, 32>(v + 16);
 }
 
-constexpr int kNumVariants = 18;
+constexpr int kNumVariants = 36;
 
 const Variant *variants() {
     static Variant table[kNumVariants];
     static bool filled = [] {
         add_variants<F16>(table);
-        add_variants<BF16>(table + 9);
+        add_variants<BF16>(table + 18);
         return true;
     }();
     (void)filled;
     return table;
 }
 
-const Variant *find_variant(int dtype, int head_dim, int block_size) {
+// The kernel for a shape: the preferred head group when it divides the head
+// count, else one head per unit.
+const Variant *find_variant(int dtype, int head_dim, int block_size, int num_heads) {
     const Variant *t = variants();
-    for (int i = 0; i < kNumVariants; ++i)
+    for (int i = 0; i < kNumVariants; i += 2)
         if (t[i].dtype == dtype && t[i].head_dim == head_dim && t[i].block_size == block_size)
-            return &t[i];
+            return (num_heads > 0 && num_heads % t[i + 1].hg == 0) ? &t[i + 1] : &t[i];
     return nullptr;
 }
 
@@ -1095,7 +1150,7 @@ cudaError_t plain_shape(const Variant *v, int device, int num_seqs, Shape *out) 
 }  // namespace
 
 bool decode_variant_supported(int dtype, int head_dim, int block_size) {
-    return find_variant(dtype, head_dim, block_size) != nullptr;
+    return find_variant(dtype, head_dim, block_size, 1) != nullptr;
 }
 
 cudaError_t prepare_decode_kernels(int device) {
@@ -1112,8 +1167,9 @@ cudaError_t prepare_decode_kernels(int device) {
     return cudaSuccess;
 }
 
-bool decode_fits(int dtype, int head_dim, int block_size, int num_seqs, int num_groups) {
-    const Variant *v = find_variant(dtype, head_dim, block_size);
+bool decode_fits(int dtype, int head_dim, int block_size, int num_heads, int num_seqs,
+                 int num_groups) {
+    const Variant *v = find_variant(dtype, head_dim, block_size, num_heads);
     int device = 0;
     if (!v || cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
         return false;
@@ -1124,7 +1180,7 @@ bool decode_fits(int dtype, int head_dim, int block_size, int num_seqs, int num_
 
 cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int block_size,
                           int num_sms, cudaStream_t stream) {
-    const Variant *v = find_variant(dtype, head_dim, block_size);
+    const Variant *v = find_variant(dtype, head_dim, block_size, args.num_heads);
     if (!v) return cudaErrorInvalidValue;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);

@@ -118,7 +118,8 @@ bool decode_variant_supported(int dtype, int head_dim, int block_size);
 // Whether a decode launch of num_seqs sequences (and num_groups shared-prefix
 // groups; -1 for none) fits the current device's shared memory (after
 // prepare_decode_kernels).
-bool decode_fits(int dtype, int head_dim, int block_size, int num_seqs, int num_groups);
+bool decode_fits(int dtype, int head_dim, int block_size, int num_heads, int num_seqs,
+                 int num_groups);
 cudaError_t prepare_decode_kernels(int device);
 
 cudaError_t launch_reshape_and_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,

@@ -72,6 +72,36 @@ def test_head_dim_block_size_variants(dev, D, B):
         assert_parity(got, ref, f"D={D} B={B} P={P}")
 
 
+@pytest.mark.parametrize("D,B", [(64, 8), (64, 16), (128, 8), (64, 32), (256, 8)])
+@pytest.mark.parametrize("H", [4, 6, 12])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_head_group_units(dev, D, B, H, dtype):
+    # Small tiles are read several heads per unit (4 heads for 1 KiB tiles, 2
+    # for 2 KiB and for the 4 KiB tiles of D 64 x B 32 and D 256 x B 8): one
+    # bulk copy moves the adjacent tiles of a block's heads, and each consumer
+    # warp keeps one head of the group.  6 heads are not a multiple of 4 (one
+    # head per unit instead); 4 and 12 divide every group size.
+    case = _ragged(f"hg{D}_{B}_{H}", [1, 2, B - 1, B, B + 1, 100, 333, 700, 1500], H=H, D=D,
+                   B=B, seed=D + B + H, dtype=dtype)
+    ref = oracle.decode_case(case)
+    for P in (0, 2 * B, 5 * B):
+        got, flags, _ = run_gpu(case, dev, P)
+        assert flags == 0
+        assert_parity(got, ref, f"{dtype} D={D} B={B} H={H} P={P}", dtype=dtype)
+
+
+@pytest.mark.parametrize("D,B", [(64, 8), (64, 16)])
+def test_head_group_units_full_size(dev, D, B):
+    # the variant batch the bench times: 64 sequences, contexts U[128, 2048],
+    # H x D = 4096 (64 heads of 64)
+    rng = np.random.default_rng(11)
+    case = workloads.build_case(f"v{D}_{B}", rng.integers(128, 2049, size=64), num_heads=64,
+                                head_dim=D, block_size=B, seed=31)
+    got, flags, _ = run_gpu(case, dev)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), f"D={D} B={B} 64 heads")
+
+
 def test_split_matches_single_pass(dev):
     rng = np.random.default_rng(17)
     case = _ragged("split", rng.integers(1, 3000, size=24), H=8)

@@ -110,22 +110,26 @@ enum Bar {
     V_FULL = 8,          // [stage]
     V_EMPTY = 11,        // [stage], one arrival per P V thread
     V_ZERO = 14,         // an item's last V tile loaded and its tail rows cleared
-    S_FULL = 15,         // [tile][buffer]
-    P_FULL = 19,         // [tile][buffer], one arrival per softmax warp
-    PV_DONE = 23,        // [tile][buffer]: the P V product reading the buffer is complete
-    O_FULL = 27,         // [tile]
-    O_EMPTY = 29,        // [tile], the epilogue has read O_t (one arrival per softmax warp)
-    MMA_DONE = 31,       // [issuing thread]
-    ITEM_FULL = 35,      // [slot] of the work-item ring
-    ITEM_EMPTY = 37,     // [slot]: the 4 MMA threads and the 8 softmax warps
-    kNumBars = 39
+    ZERO_SEEN = 15,      // both P V threads have passed the item's V_ZERO
+    S_FULL = 16,         // [tile][buffer]
+    P_FULL = 20,         // [tile][buffer], one arrival per softmax warp
+    PV_DONE = 24,        // [tile][buffer]: the P V product reading the buffer is complete
+    O_FULL = 28,         // [tile]
+    O_EMPTY = 30,        // [tile], the epilogue has read O_t (one arrival per softmax warp)
+    MMA_DONE = 32,       // [issuing thread]
+    ITEM_FULL = 36,      // [slot] of the work-item ring
+    ITEM_EMPTY = 38,     // [slot]: the 4 MMA threads and the 8 softmax warps
+    kNumBars = 40
 };
-// K_EMPTY and Q_EMPTY take one arrival from each S thread, V_EMPTY one from
-// each P V thread; a thread arrives on an
-// EMPTY barrier only after waiting for the matching FULL phase, so an
-// arrival can never count toward an earlier phase.  The per-buffer barriers
-// (S_FULL, P_FULL, PV_DONE) never run more than one phase ahead of their
-// waiters, so a parity wait cannot alias.
+// K_EMPTY and Q_EMPTY take one arrival from each S thread, V_EMPTY and
+// ZERO_SEEN one from each P V thread; a thread arrives on an EMPTY barrier
+// only after waiting for the matching FULL phase, so an arrival can never
+// count toward an earlier phase.  The per-buffer barriers (S_FULL, P_FULL,
+// PV_DONE) never run more than one phase ahead of their waiters, so a parity
+// wait cannot alias.  V_ZERO could (a short item's V tiles can all be loaded
+// while the P V threads still work on the previous item), so the TMA warp
+// completes it for item k only after ZERO_SEEN shows both P V threads past it
+// for item k - 1.
 constexpr int OFF_TMEM = OFF_BAR + kNumBars * 8;
 constexpr int OFF_FLAG = OFF_TMEM + 8;
 constexpr int OFF_ITEM = OFF_FLAG + 8;              // int[2]
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else if (i == ITEM_EMPTY || i == ITEM_EMPTY + 1)
                 count = 12;                      // the 4 MMA threads and the 8 softmax warps
             else if ((i >= K_EMPTY && i < K_EMPTY + kStages) ||
-                     (i >= V_EMPTY && i < V_EMPTY + kStages) || i == Q_EMPTY)
+                     (i >= V_EMPTY && i < V_EMPTY + kStages) || i == Q_EMPTY || i == ZERO_SEEN)
                 count = 2;                       // the 2 S threads / the 2 P V threads
             mbar_init(&bar[i], count);
         }
@@ -535,8 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++gv;
                 if (j == it.nkt - 1) {
-                    // clear V rows kmax .. end of the tile once the loads have landed
+                    // clear V rows kmax .. end of the tile once the loads have
+                    // landed (and the P V threads are past the previous item's)
                     ok = warp_all(mbar_wait(&bar[V_FULL + st], ph, abort_flag, a.err));
+                    if (ok && k > 0)
+                        ok = warp_all(mbar_wait(&bar[ZERO_SEEN], (k - 1) & 1, abort_flag, a.err));
                     if (!ok) break;
                     const int first_zero = it.kmax - j * kBN;
                     uint8_t *vt = smem + OFF_V + st * kTileKV;
@@ -662,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = last ? mbar_wait(&bar[V_ZERO], k & 1, abort_flag, a.err)
                               : mbar_wait(&bar[V_FULL + st], (g / kStages) & 1, abort_flag, a.err);
                     if (!ok) break;
+                    if (last) mbar_arrive(&bar[ZERO_SEEN]);
                     if (j < nk) {
                         const uint32_t buf = np % kSBufs;
                         ok = mbar_wait(&bar[P_FULL + t * kSBufs + buf], (np / kSBufs) & 1, abort_flag,

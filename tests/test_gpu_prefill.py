@@ -55,6 +55,23 @@ def test_ragged_prefill(dev, dtype, mode):
     assert_parity(got, ref, f"prefill {mode} {dtype}", dtype=dtype)
 
 
+def test_many_short_prompts(dev):
+    # Hundreds of items of one or two key tiles in a row: the loader then
+    # fills a whole item's V tiles while the P V threads are still on the
+    # previous item, which must not let the per-item V barrier run ahead of
+    # them.  Repeated launches on the same counters.
+    rng = np.random.default_rng(44)
+    ctx = rng.integers(1, 129, size=96)
+    ql = np.minimum(ctx, rng.integers(1, 129, size=96))
+    case = workloads.build_prefill_case("pf_short", ctx, ql, num_heads=8, head_dim=128, seed=44)
+    ref = oracle.prefill(case.q, case.k_cache, case.v_cache, case.block_tables,
+                         case.context_lens, case.query_start, case.scale)
+    for rep in range(3):
+        got, flags = run_prefill(case, dev)
+        assert flags == 0
+        assert_parity(got, ref, f"short prompts, launch {rep + 1}")
+
+
 @pytest.mark.parametrize("kind", workloads.PREFILL_WORKLOADS)
 def test_prefill_workloads_full_size(dev, kind):
     case = workloads.make_prefill_workload(kind)

@@ -99,12 +99,23 @@ __host__ __device__ constexpr int preferred_heads(int head_dim, int block_size) 
            : block_size * head_dim * 2 <= 4096 ? PA_DECODE_HG_4K : 1;
 }
 
+// Consumer warps per CTA.  1 KiB tiles (D 64 x B 8) leave each warp little
+// work per barrier and hand-off, and more warps per CTA hide that: 8 consumer
+// warps took that shape from 0.885 to 0.945 of the copy rate, while every
+// other shape lost 1-17 % with 8 (fewer CTAs, hence fewer producers, per SM).
+#ifndef PA_DECODE_NC_1K
+#define PA_DECODE_NC_1K 8
+#endif
+__host__ __device__ constexpr int consumer_warps(int head_dim, int block_size) {
+    return block_size * head_dim * 2 <= 1024 ? PA_DECODE_NC_1K : PA_DECODE_CONSUMER_WARPS;
+}
+
 template <int D, int B, int HG = 1>
 struct Cfg {
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
     static_assert(B == 8 || B == 16 || B == 32, "block_size");
     static_assert(HG == 1 || HG == 2 || HG == 4, "heads per unit");
-    static constexpr int NC = PA_DECODE_CONSUMER_WARPS;  // consumer warps
+    static constexpr int NC = consumer_warps(D, B);     // consumer warps
     static_assert(NC % HG == 0, "each head of a unit gets the same number of warps");
     static constexpr int THREADS = (NC + 1) * 32;     // + one producer warp
     static constexpr int TILE_BYTES = B * D * 2;      // one K (or V) tile, fp16

@@ -772,15 +772,17 @@ def run_prefill_op(args, local_rank):
 
 def run_shared_prefix_op(args, local_rank):
     """Time pa_decode_shared_prefix (the tensor-core prefix kernel, then the
-    suffix decode) against pa_decode on the same 128-sequence batch sharing a
-    512-token prompt, with L2 flushed before every call (so the prefix comes
-    from HBM once per call, not from the last call's L2 lines)."""
+    suffix decode) against pa_decode on the same batch sharing a 512-token
+    prompt (the shared_prefix workload, or shared_prefix_4k with
+    --workload), with L2 flushed before every call (so the prefix comes from
+    HBM once per call, not from the last call's L2 lines)."""
     import torch
     import paged_kv_cache_269_gb300 as pa
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     pa.lib()
-    case = workloads.make_workload("shared_prefix", dtype=args.dtype)
+    wl = args.workload if args.workload in ("shared_prefix", "shared_prefix_4k") else "shared_prefix"
+    case = workloads.make_workload(wl, dtype=args.dtype)
     et = torch.bfloat16 if args.dtype == "bf16" else torch.float16
 
     def t(a):
@@ -868,7 +870,7 @@ def run_shared_prefix_op(args, local_rank):
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(shared_ms, 4), "higher_is_better": True, "dtype": args.dtype,
         "data": "synthetic",
-        "config": {"workload": "shared_prefix", "num_seqs": S, "num_heads": case.num_heads,
+        "config": {"workload": wl, "num_seqs": S, "num_heads": case.num_heads,
                    "head_dim": case.head_dim, "prefix_blocks": case.shared_prefix_blocks,
                    "total_context_tokens": int(case.context_lens.sum()),
                    "partition_tokens": args.partition_tokens or 512,
@@ -885,7 +887,7 @@ def run_shared_prefix_op(args, local_rank):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": "prefix kernel + suffix decode (two launches)",
                      "unique_bytes_per_call": int(uniq), "logical_bytes_per_call": int(logical),
-                     "traffic": recorded_shared_traffic(),
+                     "traffic": recorded_shared_traffic() if wl == "shared_prefix" else None,
                      "traffic_unit": "DRAM bytes per call (both kernels)"},
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(t_begin, t_end) if sampler else None}))

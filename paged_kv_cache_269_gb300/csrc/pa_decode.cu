@@ -176,9 +176,12 @@ struct Cfg {
     // at S = 128 four CTAs per SM still fit).
     __host__ __device__ static size_t seq_ints(int num_seqs, int num_groups, int chunk_shift) {
         const size_t S = static_cast<size_t>(num_seqs);
-        if (num_groups >= 0) return 4 * S + 1 + 2 * static_cast<size_t>(num_groups) + 1 + KEYS;
-        if (chunk_shift == 0) return 2 * S + 1;
-        return ((S + (size_t{1} << chunk_shift) - 1) >> chunk_shift) + 1;
+        const size_t chunks = chunk_shift == 0 ? 0 : ((S + (size_t{1} << chunk_shift) - 1) >> chunk_shift);
+        if (num_groups >= 0) {
+            const size_t groups = 2 * static_cast<size_t>(num_groups) + 1;
+            return chunk_shift == 0 ? 4 * S + 1 + groups + KEYS : chunks + 1 + groups;
+        }
+        return chunk_shift == 0 ? 2 * S + 1 : chunks + 1;
     }
     static size_t smem_bytes(int num_seqs, int num_groups, int chunk_shift) {
         size_t n = static_cast<size_t>(OFF_SEQ) + seq_ints(num_seqs, num_groups, chunk_shift) * 4;
@@ -479,15 +482,16 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
     const int G = shared ? a.num_groups : 0;
     int *start_of = ctx_of + S;                                // [S]
     int *order = start_of + S;                                 // [S] work order: position -> s
-    int *gstart = order + S;                                   // [G + 1]
-    int *gpre = gstart + G + 1;                                // [G]
-    int *classes = gpre + G;                                   // [KEYS]
-    uint2 *defer = reinterpret_cast<uint2 *>(
-        smem + (C::OFF_SEQ + C::seq_ints(S, G, 0) * 4 + 7) / 8 * 8);   // [NC][DEFER]
-    // Chunked plain mode: prefix[c] counts the partitions of the sequences
-    // before chunk c (chunks of 2^CS sequences); ctx_of is not kept.
-    const int CS = shared ? 0 : a.chunk_shift;
+    // Chunked mode (CS > 0): prefix[c] counts the partitions of the sequences
+    // before chunk c (chunks of 2^CS sequences); no per-sequence array is
+    // kept, and in shared-prefix mode the group arrays follow the prefix.
+    const int CS = a.chunk_shift;
     const int nch = CS > 0 ? static_cast<int>((static_cast<long long>(S) + (1 << CS) - 1) >> CS) : 0;
+    int *gstart = CS > 0 ? prefix + nch + 1 : order + S;      // [G + 1]
+    int *gpre = gstart + G + 1;                                // [G]
+    int *classes = gpre + G;                                   // [KEYS] (exact mode)
+    uint2 *defer = reinterpret_cast<uint2 *>(
+        smem + (C::OFF_SEQ + C::seq_ints(S, G, CS) * 4 + 7) / 8 * 8);   // [NC][DEFER]
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -523,7 +527,8 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
             gstart[g] = __ldg(a.group_start + g);
             if (g < G) gpre[g] = __ldg(a.group_prefix_blocks + g);
         }
-        for (int s = threadIdx.x; s < S; s += blockDim.x) ctx_of[s] = a.context_lens[s];
+        if (CS == 0)
+            for (int s = threadIdx.x; s < S; s += blockDim.x) ctx_of[s] = a.context_lens[s];
         __syncthreads();
         // the group arrays: non-decreasing within [0, S], P_g within the table
         bool bad = false;
@@ -535,11 +540,31 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
         malformed = __syncthreads_or(bad) != 0;
         if (malformed && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_PREFIX);
     }
-    // partitions of a context of c tokens (c within [0, ctx_cap]); an empty
-    // context still takes one unit, which writes its zero output row
-    auto parts_of = [&](int c) {
-        const int nb = (c + B - 1) / B;
-        return nb == 0 ? 1 : (nb + TPU - 1) / TPU;
+    // partitions of a remainder of nb blocks; an empty context still takes
+    // one unit, which writes its zero output row
+    auto parts_of = [&](int nb) { return nb == 0 ? 1 : (nb + TPU - 1) / TPU; };
+    // Shared-prefix mode: the leading blocks of s that the prefix kernel's
+    // partial (slot 0) may cover, from its group, given its context length as
+    // passed (the producer still checks s's table against the group's first
+    // sequence per unit); 0 outside every group.
+    auto member_first = [&](int s, int c_in, bool report) {
+        int first = 0;
+        if (!malformed && G > 0 && gstart[0] <= s) {
+            int lo = 0, hi = G - 1;   // the last group starting at or before s
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (gstart[mid] <= s) lo = mid; else hi = mid - 1;
+            }
+            const int pb = gpre[lo];
+            if (s < gstart[lo + 1] && pb > 0) {
+                // rows the prefix kernel covers, whose context holds the prefix
+                if (c_in >= pb * B && c_in <= ctx_cap && s - gstart[lo] < a.rows_cap)
+                    first = pb;
+                else if (report)
+                    atomicOr(a.err, PA_DEVERR_PREFIX);
+            }
+        }
+        return first;
     };
     if (CS > 0) {   // one warp per chunk: its sequences' partition counts, summed
         const int nwarps = static_cast<int>(blockDim.x / 32);
@@ -548,12 +573,14 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
             for (int i = lane; i < (1 << CS); i += 32) {
                 const int s = (c << CS) + i;
                 if (s >= S) break;
-                int x = a.context_lens[s];
+                const int x_in = a.context_lens[s];
+                int x = x_in;
                 if (x < 0 || x > ctx_cap) {
                     atomicOr(a.err, PA_DEVERR_CONTEXT);
                     x = x < 0 ? 0 : ctx_cap;
                 }
-                cnt += parts_of(x);
+                const int first = shared ? member_first(s, x_in, blockIdx.x == 0) : 0;
+                cnt += parts_of((x + B - 1) / B - first);
             }
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) cnt += __shfl_xor_sync(kFull, cnt, off);
@@ -570,22 +597,7 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
         const int nblk = (c + B - 1) / B;
         int first = 0;
         if (shared) {
-            if (!malformed && G > 0 && gstart[0] <= s) {
-                int lo = 0, hi = G - 1;   // the last group starting at or before s
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (gstart[mid] <= s) lo = mid; else hi = mid - 1;
-                }
-                const int pb = gpre[lo];
-                if (s < gstart[lo + 1] && pb > 0) {
-                    // rows the prefix kernel covers, whose context holds the prefix
-                    if (c_in >= pb * B && c_in <= ctx_cap && s - gstart[lo] < a.rows_cap) {
-                        first = pb;
-                    } else if (blockIdx.x == 0) {
-                        atomicOr(a.err, PA_DEVERR_PREFIX);
-                    }
-                }
-            }
+            first = member_first(s, c_in, blockIdx.x == 0);
             start_of[s] = first;
         }
         const int rest = nblk - first;
@@ -593,7 +605,7 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
         if (!shared) prefix[s + 1] = rest == 0 ? 1 : (rest + TPU - 1) / TPU;  // partitions of s
     }
     __syncthreads();
-    if (shared && warp == C::NC) {
+    if (shared && CS == 0 && warp == C::NC) {
         // Work order, shared-prefix mode: longest first unit first (a stable
         // counting sort, descending, over KEYS length classes), so that the
         // queue ends on short units.  Plain decode keeps sequence order (its
@@ -642,7 +654,7 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
         for (int base = 0; base < NE; base += 32) {
             const int s = base + lane;
             int v = 0;
-            if (s < NE && shared) {   // partitions of the sequence in place s
+            if (s < NE && shared && CS == 0) {   // partitions of the sequence in place s
                 const int r = order[s];
                 const int rest = (ctx_of[r] + B - 1) / B - start_of[r];
                 v = rest == 0 ? 1 : (rest + TPU - 1) / TPU;
@@ -683,12 +695,13 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
                 const int mid = (lo + hi + 1) >> 1;
                 if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
             }
-            int s, p, np, ctx;
+            int s, p, np, ctx, first = 0;
             if (CS == 0) {
                 s = shared ? order[lo] : lo;
                 p = g - prefix[lo];
                 np = prefix[lo + 1] - prefix[lo];
                 ctx = ctx_of[s];
+                if (shared) first = start_of[s];
             } else {
                 // chunk lo: each lane takes 2^(CS-5) consecutive sequences,
                 // a warp scan of their partition counts finds the lane whose
@@ -697,10 +710,18 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
                 const int rem = g - prefix[lo];
                 const int per_lane = 1 << (CS - 5);
                 const int sb = (lo << CS) + lane * per_lane;
+                // partitions of sequence q (and its prefix blocks, shared mode)
+                auto seq_parts = [&](int q, int &c, int &f) {
+                    const int x_in = __ldg(a.context_lens + q);
+                    c = min(max(x_in, 0), ctx_cap);
+                    f = shared ? member_first(q, x_in, false) : 0;
+                    return parts_of((c + B - 1) / B - f);
+                };
                 int tot = 0;
                 for (int i = 0; i < per_lane; ++i) {
                     if (sb + i >= S) break;
-                    tot += parts_of(min(max(__ldg(a.context_lens + sb + i), 0), ctx_cap));
+                    int c, f;
+                    tot += seq_parts(sb + i, c, f);
                 }
                 int inc = tot;
 #pragma unroll
@@ -714,13 +735,13 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
                     continue;
                 }
                 const int L = __ffs(hit) - 1;
-                int fs = -1, fp = 0, fnp = 1, fctx = 0;
+                int fs = -1, fp = 0, fnp = 1, fctx = 0, ffirst = 0;
                 if (lane == L) {
                     int r = rem - (inc - tot);
                     for (int i = 0; i < per_lane && sb + i < S; ++i) {
-                        const int c = min(max(__ldg(a.context_lens + sb + i), 0), ctx_cap);
-                        const int n = parts_of(c);
-                        if (r < n) { fs = sb + i; fp = r; fnp = n; fctx = c; break; }
+                        int c, f;
+                        const int n = seq_parts(sb + i, c, f);
+                        if (r < n) { fs = sb + i; fp = r; fnp = n; fctx = c; ffirst = f; break; }
                         r -= n;
                     }
                 }
@@ -728,13 +749,13 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
                 p = __shfl_sync(kFull, fp, L);
                 np = __shfl_sync(kFull, fnp, L);
                 ctx = __shfl_sync(kFull, fctx, L);
+                first = __shfl_sync(kFull, ffirst, L);
                 if (s < 0) {
                     if (lane == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
                     continue;
                 }
             }
             const int nblk = (ctx + B - 1) / B;
-            const int first = shared ? start_of[s] : 0;
             bool pre = first > 0;
             int leader = s;
             if (pre) {   // the group's first sequence: the last group start at or before s
@@ -1106,12 +1127,12 @@ const Variant *find_variant(int dtype, int head_dim, int block_size, int num_hea
 constexpr int kMaxDevices = 64;
 int g_max_dynamic_smem[kMaxDevices] = {0};
 
-// Launch shape of one plain-mode decode: the sequence-state layout, its
-// shared memory and the CTAs per SM it allows.  The last shape computed per
-// device and variant is kept, so repeated calls with the same batch size
-// query the occupancy calculator once.
+// Launch shape of one decode: the sequence-state layout, its shared memory
+// and the CTAs per SM it allows.  The last shape computed per device and
+// variant is kept, so repeated calls with the same batch (and groups) query
+// the occupancy calculator once.
 struct Shape {
-    int num_seqs = -1, chunk_shift = 0, per_sm = 0;
+    int num_seqs = -1, num_groups = -2, chunk_shift = 0, per_sm = 0;
     size_t smem = 0;
 };
 Shape g_last_shape[kMaxDevices][kNumVariants];
@@ -1122,26 +1143,30 @@ cudaError_t occupancy(const Variant *v, size_t smem, int *per_sm) {
 }
 
 // Per-sequence state (chunk_shift 0) while it leaves the CTAs per SM at what
-// the fixed footprint alone allows; otherwise the smallest chunk of 2^c
-// sequences (c >= 5) that does, or one chunk for the whole batch.
-cudaError_t plain_shape(const Variant *v, int device, int num_seqs, Shape *out) {
+// the fixed footprint (and the group arrays) alone allow; otherwise the
+// smallest chunk of 2^c sequences (c >= 5) that does, or one chunk for the
+// whole batch.  num_groups < 0: plain mode.
+cudaError_t decode_shape(const Variant *v, int device, int num_seqs, int num_groups, Shape *out) {
     const int vi = static_cast<int>(v - variants());
     {
         std::lock_guard<std::mutex> lock(g_shape_mutex);
         const Shape &c = g_last_shape[device][vi];
-        if (c.num_seqs == num_seqs) {
+        if (c.num_seqs == num_seqs && c.num_groups == num_groups) {
             *out = c;
             return cudaSuccess;
         }
     }
     int best = 0;
-    cudaError_t e = occupancy(v, v->smem_bytes(1, -1, 30), &best);
+    const size_t least = v->smem_bytes(1, num_groups, 30);
+    if (least > static_cast<size_t>(g_max_dynamic_smem[device])) return cudaErrorInvalidConfiguration;
+    cudaError_t e = occupancy(v, least, &best);
     if (e != cudaSuccess) return e;
     Shape sh;
     sh.num_seqs = num_seqs;
+    sh.num_groups = num_groups;
     for (int cs = 0;; cs = cs == 0 ? 5 : cs + 1) {
         sh.chunk_shift = cs;
-        sh.smem = v->smem_bytes(num_seqs, -1, cs);
+        sh.smem = v->smem_bytes(num_seqs, num_groups, cs);
         const bool one_chunk = cs >= 30 || (cs > 0 && (num_seqs >> cs) == 0);
         if (sh.smem > static_cast<size_t>(g_max_dynamic_smem[device])) {
             if (one_chunk) return cudaErrorInvalidConfiguration;
@@ -1184,9 +1209,9 @@ bool decode_fits(int dtype, int head_dim, int block_size, int num_heads, int num
     int device = 0;
     if (!v || cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
         return false;
-    if (num_groups < 0) return true;   // plain mode always has a fitting layout
-    return v->smem_bytes(num_seqs, num_groups, 0) <=
-           static_cast<size_t>(g_max_dynamic_smem[device]);
+    // some layout fits unless the group arrays alone exceed the shared memory
+    Shape sh;
+    return decode_shape(v, device, num_seqs, num_groups, &sh) == cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int block_size,
@@ -1198,24 +1223,13 @@ cudaError_t launch_decode(const DecodeArgs &args, int dtype, int head_dim, int b
     if (e != cudaSuccess) return e;
     if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
     DecodeArgs la = args;
-    size_t smem = 0;
-    int per_sm = 0;
-    if (args.group_start != nullptr) {
-        la.chunk_shift = 0;
-        smem = v->smem_bytes(args.num_seqs, args.num_groups, 0);
-        if (smem > static_cast<size_t>(g_max_dynamic_smem[device]))
-            return cudaErrorInvalidConfiguration;
-        e = occupancy(v, smem, &per_sm);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    } else {
-        Shape sh;
-        e = plain_shape(v, device, args.num_seqs, &sh);
-        if (e != cudaSuccess) return e;
-        la.chunk_shift = sh.chunk_shift;
-        smem = sh.smem;
-        per_sm = sh.per_sm;
-    }
+    Shape sh;
+    e = decode_shape(v, device, args.num_seqs, args.group_start != nullptr ? args.num_groups : -1,
+                     &sh);
+    if (e != cudaSuccess) return e;
+    la.chunk_shift = sh.chunk_shift;
+    const size_t smem = sh.smem;
+    const int per_sm = sh.per_sm;
     // Persistent grid; never more CTAs than the most work units there can be.
     const long long max_units = static_cast<long long>(args.num_seqs) * args.num_heads * args.max_parts;
     long long grid = static_cast<long long>(per_sm) * num_sms;

@@ -257,3 +257,44 @@ def test_output_in_pinned_host_memory(dev):
     with pytest.raises(ValueError):        # pageable host memory is refused
         pa.decode(torch.empty(case.q.shape, dtype=torch.float16), d["q"], d["k_cache"],
                   d["v_cache"], d["block_tables"], d["context_lens"], case.scale)
+
+
+@pytest.mark.parametrize("n_groups,members,partition_tokens", [(6, 700, 0), (400, 8, 64)])
+def test_serving_size_batches(dev, n_groups, members, partition_tokens):
+    # Thousands of sequences: each CTA keeps the group arrays and one
+    # partition count per chunk of sequences instead of per-sequence state,
+    # and derives a sequence's prefix coverage from its group when it needs
+    # it.  Some groups share nothing; 64-token partitions split suffixes.
+    rng = np.random.default_rng(71 + n_groups)
+    layout = []
+    for _ in range(n_groups):
+        P = int(rng.integers(0, 6))
+        layout.append((P, [int(c) for c in P * 16 + rng.integers(0, 300, members)]))
+    case, gs, gp = workloads.build_grouped_case(f"sp_big{n_groups}", layout, num_heads=2,
+                                                head_dim=128, seed=71 + n_groups)
+    got, flags = run_shared(case, gs, gp, dev, partition_tokens=partition_tokens)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), f"{n_groups} groups x {members}")
+
+
+def test_one_group_of_4096(dev):
+    # one 512-token prompt shared by 4096 requests
+    rng = np.random.default_rng(73)
+    layout = [(32, [int(c) for c in 512 + rng.integers(0, 200, 4096)])]
+    case, gs, gp = workloads.build_grouped_case("sp_4096", layout, num_heads=2, head_dim=128,
+                                                seed=73)
+    got, flags = run_shared(case, gs, gp, dev)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), "one group of 4096")
+
+
+def test_shared_prefix_4k_full_size(dev):
+    # the shared_prefix_4k workload (4096 sequences x 8 heads, one 512-token
+    # prompt) through the shared-prefix call, as the bench times it
+    case = workloads.make_workload("shared_prefix_4k")
+    S = case.num_seqs
+    gs = np.array([0, S], dtype=np.int32)
+    gp = np.array([case.shared_prefix_blocks], dtype=np.int32)
+    got, flags = run_shared(case, gs, gp, dev, max_group_size=S)
+    assert flags == 0
+    assert_parity(got, oracle.decode_case(case), "shared_prefix_4k")

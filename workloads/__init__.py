@@ -429,7 +429,7 @@ def duplicate_prefix(case: DecodeCase) -> DecodeCase:
 # ----------------------------------------------------------------------------
 
 WORKLOADS = ("tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx", "cb_mix_1k",
-             "cb_mix_4k")
+             "cb_mix_4k", "shared_prefix_4k")
 
 
 def make_workload(kind: str, seed: Optional[int] = None, **kw) -> DecodeCase:
@@ -451,9 +451,11 @@ def make_workload(kind: str, seed: Optional[int] = None, **kw) -> DecodeCase:
                   (32 heads, D 128; 7.8 GB of K/V).
     cb_mix_4k     the same recipe at 4096 sequences, with 8 heads of D 128 (the
                   K/V of a layer with 8 key/value heads; 7.8 GB of K/V).
+    shared_prefix_4k  shared_prefix's recipe (one 512-token prompt, private
+                  suffixes of U[16, 512] tokens) at 4096 sequences, 8 heads.
     """
     seeds = {"tiny": 1, "llama7b_b64": 2, "cb_mix": 3, "shared_prefix": 4, "long_ctx": 5,
-             "cb_mix_1k": 6, "cb_mix_4k": 7}
+             "cb_mix_1k": 6, "cb_mix_4k": 7, "shared_prefix_4k": 8}
     if kind not in seeds:
         raise KeyError(kind)
     seed = seeds[kind] if seed is None else seed
@@ -478,9 +480,10 @@ def make_workload(kind: str, seed: Optional[int] = None, **kw) -> DecodeCase:
         gen = np.minimum(rng.geometric(1.0 / 200.0, size=n), 1000)
         return build_case(kind, prompt + gen, num_heads=heads, head_dim=128, seed=seed,
                           max_blocks_per_seq=blocks_needed(512 + 1000), **kw)
-    if kind == "shared_prefix":
-        suffix = rng.integers(16, 512, size=128, endpoint=True)
-        return build_case(kind, 512 + suffix, num_heads=32, head_dim=128, seed=seed,
+    if kind in ("shared_prefix", "shared_prefix_4k"):
+        n, heads = (128, 32) if kind == "shared_prefix" else (4096, 8)
+        suffix = rng.integers(16, 512, size=n, endpoint=True)
+        return build_case(kind, 512 + suffix, num_heads=heads, head_dim=128, seed=seed,
                           max_blocks_per_seq=64, shared_prefix_blocks=32, **kw)
     # long_ctx
     return build_case(kind, np.full(8, 32768), num_heads=32, head_dim=128, seed=seed,

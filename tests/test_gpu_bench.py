@@ -50,6 +50,12 @@ def test_step_line_has_the_contract_keys(gpu):
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert e["value"] < d["value"] * 1.05              # the host link can only cost
     assert d["gpu_launches"] == 2 * d["steps"]
+    # the decode's own duration comes from a long decode-only loop, and a
+    # kernel cannot take longer than the step it sits in
+    assert r["launches_timed"] >= 200
+    assert d["decode_ms"] <= d["ms_per_step"]
+    clk = d["clocks"]
+    assert clk is not None and clk["samples"] >= 5 and clk["sm_mhz"] > 0
 
 
 def test_shared_prefix_line(gpu):

@@ -121,11 +121,11 @@ def recorded_prefill_traffic(workload):
 SHARED_SOURCES = DECODE_SOURCES + PREFILL_SOURCES
 
 
-def recorded_shared_traffic():
+def recorded_shared_traffic(workload):
     """DRAM bytes (read + write) of one shared-prefix call (the prefix kernel
-    plus the suffix decode) from the committed ncu summary, if it was taken on
-    the current sources of both kernels; else None."""
-    path = os.path.join(ROOT, "profiles", "pa_decode_shared_prefix.txt")
+    plus the suffix decode) on a workload from the committed ncu summary, if
+    it was taken on the current sources of both kernels; else None."""
+    path = os.path.join(ROOT, "profiles", f"pa_shared_prefix_call_{workload}.txt")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -887,7 +887,7 @@ def run_shared_prefix_op(args, local_rank):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": "prefix kernel + suffix decode (two launches)",
                      "unique_bytes_per_call": int(uniq), "logical_bytes_per_call": int(logical),
-                     "traffic": recorded_shared_traffic() if wl == "shared_prefix" else None,
+                     "traffic": recorded_shared_traffic(wl),
                      "traffic_unit": "DRAM bytes per call (both kernels)"},
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(t_begin, t_end) if sampler else None}))

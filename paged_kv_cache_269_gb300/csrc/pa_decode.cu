@@ -519,16 +519,25 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
     // where they are read (and to the end).
     if (!shared) grid_dependency_wait();
     allow_dependents_to_launch();
+    // the producer's first unit, grabbed now so that the grab's round trip
+    // overlaps the prologue (every earlier call on the stream, which resets
+    // the queue at its end, is complete here)
+    uint32_t first_grab = 0;
+    if (warp == C::NC && lane == 0) first_grab = atomicAdd(&a.counters[0], 1u);
     const int ctx_cap = a.max_blocks_per_seq * B;
     bool malformed = false;
     if (shared) {
-        // one round of global loads: the group arrays and the lengths
-        for (int g = threadIdx.x; g <= G; g += blockDim.x) {
-            gstart[g] = __ldg(a.group_start + g);
-            if (g < G) gpre[g] = __ldg(a.group_prefix_blocks + g);
+        // one round of global loads: the group arrays and the lengths, each
+        // thread's loads all issued before any is stored
+        const int n_in = max(G + 1, CS == 0 ? S : 0);
+        for (int i = threadIdx.x; i < n_in; i += blockDim.x) {
+            const int gs_i = i <= G ? __ldg(a.group_start + i) : 0;
+            const int gp_i = i < G ? __ldg(a.group_prefix_blocks + i) : 0;
+            const int c_i = CS == 0 && i < S ? a.context_lens[i] : 0;
+            if (i <= G) gstart[i] = gs_i;
+            if (i < G) gpre[i] = gp_i;
+            if (CS == 0 && i < S) ctx_of[i] = c_i;
         }
-        if (CS == 0)
-            for (int s = threadIdx.x; s < S; s += blockDim.x) ctx_of[s] = a.context_lens[s];
         __syncthreads();
         // the group arrays: non-decreasing within [0, S], P_g within the table
         bool bad = false;
@@ -605,18 +614,69 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
         if (!shared) prefix[s + 1] = rest == 0 ? 1 : (rest + TPU - 1) / TPU;  // partitions of s
     }
     __syncthreads();
-    if (shared && CS == 0 && warp == C::NC) {
-        // Work order, shared-prefix mode: longest first unit first (a stable
-        // counting sort, descending, over KEYS length classes), so that the
-        // queue ends on short units.  Plain decode keeps sequence order (its
-        // concurrent CTAs then share the L2 lines of common blocks); here the
-        // common blocks are the prefix kernel's.  Every CTA derives the same
-        // order: counts, then placement in sequence order within a class.
-        static_assert(C::KEYS == 32, "one length class per lane");
-        auto key_of = [&](int s) {
-            const int rest = (ctx_of[s] + B - 1) / B - start_of[s];
-            return min(rest, TPU) * (C::KEYS - 1) / TPU;
-        };
+    // Work order, shared-prefix mode: longest first unit first (a stable
+    // counting sort, descending, over KEYS length classes), so that the queue
+    // ends on short units.  Plain decode keeps sequence order (its concurrent
+    // CTAs then share the L2 lines of common blocks); here the common blocks
+    // are the prefix kernel's.  Every CTA derives the same order: class sizes,
+    // then placement in sequence order within a class.
+    static_assert(C::KEYS == 32, "one length class per lane");
+    auto key_of = [&](int s) {
+        const int rest = (ctx_of[s] + B - 1) / B - start_of[s];
+        return min(rest, TPU) * (C::KEYS - 1) / TPU;
+    };
+    // All warps sort, one chunk of 32 sequences each, with per-chunk class
+    // sizes kept in the merge buffer (unused until the first unit ends); a
+    // batch whose sizes do not fit there is sorted by one warp.
+    const int nch32 = (S + 31) / 32;
+    const bool wide_sort = shared && CS == 0 && nch32 * C::KEYS <= C::ND * C::NC * D;
+    if (wide_sort) {
+        int *first_of = reinterpret_cast<int *>(merge_acc);   // [nch32][KEYS]
+        const int nwarps = static_cast<int>(blockDim.x / 32);
+        for (int c = warp; c < nch32; c += nwarps) {   // the classes' sizes in chunk c
+            const int s = c * 32 + lane;
+            first_of[c * C::KEYS + lane] = 0;
+            __syncwarp();
+            const unsigned active = __ballot_sync(kFull, s < S);
+            if (s < S) {
+                const int k = key_of(s);
+                const unsigned peers = __match_any_sync(active, k);
+                if (lane == __ffs(peers) - 1) first_of[c * C::KEYS + k] = __popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // first place of (class k, chunk c): the classes longer than k,
+            // then class k in the chunks before c; lane 0 holds the longest
+            const int k = C::KEYS - 1 - lane;
+            int total = 0;
+            for (int c = 0; c < nch32; ++c) total += first_of[c * C::KEYS + k];
+            int v = total;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(kFull, v, off);
+                if (lane >= off) v += y;
+            }
+            int place = v - total;
+            for (int c = 0; c < nch32; ++c) {
+                const int n = first_of[c * C::KEYS + k];
+                first_of[c * C::KEYS + k] = place;
+                place += n;
+            }
+        }
+        __syncthreads();
+        for (int c = warp; c < nch32; c += nwarps) {   // placement
+            const int s = c * 32 + lane;
+            const unsigned active = __ballot_sync(kFull, s < S);
+            if (s < S) {
+                const int k = key_of(s);
+                const unsigned peers = __match_any_sync(active, k);
+                order[first_of[c * C::KEYS + k] + __popc(peers & ((1u << lane) - 1u))] = s;
+            }
+        }
+        __syncthreads();
+    } else if (shared && CS == 0 && warp == C::NC) {
         classes[lane] = 0;
         __syncwarp();
         for (int s = lane; s < S; s += 32) atomicAdd(&classes[key_of(s)], 1);
@@ -682,8 +742,7 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
         uint32_t kq = 0;  // tiles issued
         uint32_t dq = 0;  // unit descriptors issued
         bool ok = true;
-        uint32_t pending = 0;
-        if (lane == 0) pending = atomicAdd(&a.counters[0], 1u);
+        uint32_t pending = first_grab;
         while (true) {
             const uint32_t u = __shfl_sync(kFull, pending, 0);
             if (u >= num_units) break;
@@ -766,19 +825,27 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
                 }
                 leader = gstart[glo];
             }
+            const int32_t *srow = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
+            // the first table slice, loaded as it is if the prefix partial
+            // applies, together with the check below
+            int t0 = (pre || p > 0) ? first + p * TPU : 0;
+            int nt = max(0, min(nblk, first + (p + 1) * TPU) - t0);
+            int phys_first = lane < min(nt, 32) ? __ldg(srow + t0 + lane) : 0;
             if (pre && leader != s) {
                 // the prefix partial is s's only if s's first blocks are its
                 // group's; otherwise the first partition takes them on
-                const int32_t *mine = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
                 const int32_t *lead =
                     a.block_tables + static_cast<size_t>(leader) * a.max_blocks_per_seq;
                 bool same = true;
-                for (int b = lane; b < first; b += 32) same = same && __ldg(mine + b) == __ldg(lead + b);
+                for (int b = lane; b < first; b += 32) same = same && __ldg(srow + b) == __ldg(lead + b);
                 pre = __all_sync(kFull, same);
                 if (!pre && lane == 0 && h == 0 && p == 0) atomicOr(a.err, PA_DEVERR_PREFIX);
+                if (!pre && p == 0) {   // the first partition starts at block 0 after all
+                    t0 = 0;
+                    nt = max(0, min(nblk, first + TPU));
+                    phys_first = lane < min(nt, 32) ? __ldg(srow + lane) : 0;
+                }
             }
-            const int t0 = (pre || p > 0) ? first + p * TPU : 0;
-            const int nt = max(0, min(nblk, first + (p + 1) * TPU) - t0);
 
             const int slot = static_cast<int>(dq % C::ND);
             bool w_ok = mbar_wait(&desc_empty[slot], ((dq / C::ND) & 1u) ^ 1u, abort_flag, a.err);
@@ -794,10 +861,11 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
             }
             ++dq;
 
-            const int32_t *row = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + t0;
+            const int32_t *row = srow + t0;
             for (int j0 = 0; j0 < nt && ok; j0 += 32) {
                 const int n = min(32, nt - j0);
-                const int phys_lane = lane < n ? __ldg(row + j0 + lane) : 0;
+                const int phys_lane =
+                    j0 == 0 ? phys_first : (lane < n ? __ldg(row + j0 + lane) : 0);
                 if constexpr (C::R == 1) {
                     for (int jj = 0; jj < n; ++jj) {
                         const int phys = __shfl_sync(kFull, phys_lane, jj);

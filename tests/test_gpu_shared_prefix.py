@@ -89,6 +89,25 @@ def test_ragged_groups(dev, dtype, partition_tokens):
     assert int(ctr.count_nonzero()) == 0        # the counters are left zeroed
 
 
+@pytest.mark.parametrize("partition_tokens", [0, 256])
+def test_work_order_over_several_chunks(dev, partition_tokens):
+    """140 sequences (four full 32-sequence chunks and a ragged one) in the
+    per-sequence layout: the longest-first work order is built by several
+    warps, one chunk each, and must come out the same in every CTA."""
+    rng = np.random.default_rng(23)
+    layout = [(4, [int(c) for c in rng.integers(70, 900, 50)]), (0, [30, 700]),
+              (6, [int(c) for c in rng.integers(97, 620, 60)]),
+              (2, [int(c) for c in rng.integers(33, 1200, 28)])]
+    case, gs, gp = workloads.build_grouped_case("order", layout, num_heads=4, head_dim=128,
+                                                seed=23)
+    ctr, ws = _buffers(dev, case, partition_tokens)
+    for _ in range(2):
+        got, flags = run_shared(case, gs, gp, dev, partition_tokens, counters=ctr, workspace=ws)
+        assert flags == 0
+        assert_parity(got, oracle.decode_case(case), f"order P={partition_tokens}")
+        assert int(ctr.count_nonzero()) == 0
+
+
 def test_shared_prefix_workload_full_size(dev):
     """The 128-sequence, 512-token-prompt batch, in the launch configuration the
     benchmark times: one group of 128 sharing 32 blocks."""

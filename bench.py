@@ -64,6 +64,9 @@ def parse():
                    help="--impl reference: oracle time the whole run is sized for")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other workloads' decode (and shared-prefix call) timings "
+                        "that the step line carries under \"workloads\"")
     p.add_argument("--flush-l2", action="store_true",
                    help="write a 256 MiB buffer, then read another, before every step so "
                         "shared blocks start cold and L2 holds no dirty lines; "
@@ -385,6 +388,150 @@ ROOFLINE_MIN_LAUNCHES = 200     # decode-only launches timed for the roofline
 ROOFLINE_MIN_SECONDS = 0.5      # ... and at least this long, so the clock sampler sees it
 
 
+SIDE_WORKLOADS = ("tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx", "cb_mix_1k",
+                  "cb_mix_4k")
+SIDE_SHARED = ("shared_prefix", "shared_prefix_4k")
+SIDE_MIN_SECONDS = 0.25
+
+
+def side_workloads(args, dev):
+    """The other decode workloads, timed in the same run as the step line:
+    each workload's decode alone (its block tables and lengths, q and caches
+    drawn on the device), back to back between two events, at least
+    ROOFLINE_MIN_LAUNCHES launches and SIDE_MIN_SECONDS; then the
+    shared-prefix call against pa_decode on each shared-prefix batch, one call
+    per L2 flush.  Fractions are of the measured HBM copy rate."""
+    import torch
+    import paged_kv_cache_269_gb300 as pa
+    peak, _ = measured_peaks()
+    et = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+    dt = 1 if args.dtype == "bf16" else 0
+    stream = torch.cuda.Stream(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+
+    def on_device(case):
+        t = {k: torch.from_numpy(np.ascontiguousarray(getattr(case, k))).to(dev)
+             for k in ("block_tables", "context_lens")}
+        for k in ("q", "k_cache", "v_cache"):
+            t[k] = torch.randn(getattr(case, k).shape, generator=gen, device=dev, dtype=et)
+        return t
+
+    def decode_fn(case, d):
+        ws = torch.empty(max(16, pa.decode_workspace_bytes(
+            case.num_seqs, case.num_heads, case.head_dim, case.block_size, case.num_blocks,
+            case.max_blocks_per_seq, args.partition_tokens, dtype=dt)), dtype=torch.uint8,
+            device=dev)
+        ctr = torch.zeros(pa.decode_counters_bytes(case.num_seqs, case.num_heads) // 4,
+                          dtype=torch.int32, device=dev)
+        out = torch.empty(case.q.shape, dtype=et, device=dev)
+        return lambda: pa.decode(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                 d["context_lens"], case.scale,
+                                 partition_tokens=args.partition_tokens, workspace=ws,
+                                 counters=ctr, stream=stream)
+
+    res = {}
+    sampler = ClockSampler(dev.index or 0) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t_begin = time.time()
+    for w in SIDE_WORKLOADS:
+        if w == args.workload:
+            continue
+        case = workloads.make_workload(w, values=False, dtype=args.dtype)
+        d = on_device(case)
+        fn = decode_fn(case, d)
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        est = e0.elapsed_time(e1) / 10
+        n = min(200000, max(ROOFLINE_MIN_LAUNCHES, int(SIDE_MIN_SECONDS * 1e3 / max(est, 1e-3)) + 1))
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / n
+        if pa.device_errors(stream=stream):
+            raise RuntimeError(f"device error in the {w} decode")
+        alg = workloads.decode_algorithmic_bytes(case)
+        uq = workloads.decode_unique_bytes(case)
+        res[w] = {"decode_ms": round(ms, 4), "gbs": round(alg / (ms * 1e-3) / 1e9, 2),
+                  "frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
+                  "unique_gbs": round(uq / (ms * 1e-3) / 1e9, 2),
+                  "unique_frac": round(uq / (ms * 1e-3) / 1e9 / peak, 4),
+                  "num_seqs": case.num_seqs, "num_heads": case.num_heads, "launches": n}
+        del d, fn
+        torch.cuda.empty_cache()
+    flush = L2Flush(torch, dev)
+    for w in SIDE_SHARED:
+        case = workloads.make_workload(w, values=False, dtype=args.dtype)
+        d = on_device(case)
+        S = case.num_seqs
+        gs = torch.tensor([0, S], dtype=torch.int32, device=dev)
+        gp = torch.tensor([case.shared_prefix_blocks], dtype=torch.int32, device=dev)
+        ws = torch.empty(pa.decode_shared_prefix_workspace_bytes(
+            S, case.num_heads, case.head_dim, case.block_size, case.num_blocks,
+            case.max_blocks_per_seq, args.partition_tokens, dtype=dt), dtype=torch.uint8,
+            device=dev)
+        ctr = torch.zeros(pa.decode_shared_prefix_counters_bytes(
+            S, case.num_heads, case.head_dim, case.block_size, case.num_blocks) // 4,
+            dtype=torch.int32, device=dev)
+        out = torch.empty(case.q.shape, dtype=et, device=dev)
+
+        def shared():
+            pa.decode_shared_prefix(out, d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                    d["context_lens"], case.scale, gs, gp, max_group_size=S,
+                                    partition_tokens=args.partition_tokens, counters=ctr,
+                                    workspace=ws, stream=stream)
+
+        plain = decode_fn(case, d)
+
+        def per_call(fn, calls):
+            for _ in range(3):
+                fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(calls)]
+            for a0, a1 in evs:
+                flush(torch, stream)
+                a0.record(stream)
+                fn()
+                a1.record(stream)
+            torch.cuda.synchronize(dev)
+            return sum(a0.elapsed_time(a1) for a0, a1 in evs) / calls
+
+        calls = 100 if S <= 256 else 20
+        ms_s, ms_p = per_call(shared, calls), per_call(plain, calls)
+        if pa.device_errors(stream=stream):
+            raise RuntimeError(f"device error in the {w} shared-prefix call")
+        uq = workloads.decode_unique_bytes(case)
+        res[w + "_shared_call"] = {
+            "ms": round(ms_s, 4), "unique_gbs": round(uq / (ms_s * 1e-3) / 1e9, 2),
+            "unique_frac": round(uq / (ms_s * 1e-3) / 1e9 / peak, 4),
+            "plain_decode_ms": round(ms_p, 4), "speedup_vs_plain": round(ms_p / ms_s, 3),
+            "num_seqs": S, "num_heads": case.num_heads, "calls": calls}
+        del d
+        torch.cuda.empty_cache()
+    t_end = time.time()
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+    return {"method": "decode alone: back-to-back launches between two events (at least "
+                      f"{ROOFLINE_MIN_LAUNCHES} and {SIDE_MIN_SECONDS} s), inputs larger than L2 "
+                      "except tiny (whose launches are paced by the host's Python calls, not the "
+                      "GPU); shared-prefix call and pa_decode on its batch: one call per "
+                      "L2 flush (256 MiB write, then 256 MiB read), mean over the calls; q and "
+                      "caches drawn on the device; fractions of the measured HBM copy rate",
+            "dtype": args.dtype, "results": res,
+            "clocks": sampler.summary(t_begin, t_end, "these timings") if sampler else None}
+
+
 def run_native(args, rank, world, local_rank):
     import torch
     import paged_kv_cache_269_gb300 as pa
@@ -615,6 +762,9 @@ def run_native(args, rank, world, local_rank):
 
     if rank != 0:
         return
+    # the other workloads, timed in this run (one GPU runs them; at N > 1 the
+    # ranks would only repeat them)
+    side = side_workloads(args, dev) if world == 1 and not args.no_workloads else None
     peak, peak_kind = measured_peaks()
     dec_bytes = workloads.decode_algorithmic_bytes(case)
     uniq_bytes = workloads.decode_unique_bytes(case)
@@ -651,6 +801,7 @@ def run_native(args, rank, world, local_rank):
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(t_begin, t_end, "timed steps and the decode launches timed "
                                   "for the roofline") if sampler else None,
+        "workloads": side,
     }
     print(json.dumps(line))
 

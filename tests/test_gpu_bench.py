@@ -56,6 +56,15 @@ def test_step_line_has_the_contract_keys(gpu):
     assert d["decode_ms"] <= d["ms_per_step"]
     clk = d["clocks"]
     assert clk is not None and clk["samples"] >= 5 and clk["sm_mhz"] > 0
+    # the other workloads, timed in the same run
+    side = d["workloads"]["results"]
+    for w in ("tiny", "cb_mix", "shared_prefix", "long_ctx", "cb_mix_1k", "cb_mix_4k"):
+        assert side[w]["decode_ms"] > 0 and side[w]["launches"] >= 200, w
+        if w != "tiny":                                   # HBM-bound: a copy-rate fraction
+            assert 0.3 < side[w]["unique_frac"] < 1.3, (w, side[w])
+    for w in ("shared_prefix", "shared_prefix_4k"):
+        c = side[w + "_shared_call"]
+        assert c["speedup_vs_plain"] > 1.0 and 0.3 < c["unique_frac"] < 1.3, (w, c)
 
 
 def test_shared_prefix_line(gpu):

@@ -58,6 +58,21 @@ constexpr int clamp_int(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? 
 #ifndef PA_DECODE_STAGE_KIB
 #define PA_DECODE_STAGE_KIB 48
 #endif
+// Ring budgets of two small-tile shapes, from a sweep of 32, 40 and 48 KiB:
+// D 64 x B 8 at 40 KiB fits four CTAs per SM (56 registers, no spill) instead
+// of three (+0.3 %), D 64 x B 16 gains 0.5 % at 32 KiB; every other shape is
+// best at 48 KiB (D 128 x B 8 lost 1 % at 32).
+#ifndef PA_DECODE_STAGE_KIB_D64_B8
+#define PA_DECODE_STAGE_KIB_D64_B8 40
+#endif
+#ifndef PA_DECODE_STAGE_KIB_D64_B16
+#define PA_DECODE_STAGE_KIB_D64_B16 32
+#endif
+__host__ __device__ constexpr int stage_budget_kib(int head_dim, int block_size) {
+    return head_dim == 64 && block_size == 8    ? PA_DECODE_STAGE_KIB_D64_B8
+           : head_dim == 64 && block_size == 16 ? PA_DECODE_STAGE_KIB_D64_B16
+                                                : PA_DECODE_STAGE_KIB;
+}
 #ifndef PA_DECODE_MAX_STAGES
 #define PA_DECODE_MAX_STAGES 16
 #endif
@@ -127,7 +142,7 @@ struct Cfg {
     static_assert(32 % R == 0, "a stage never straddles a 32-entry table slice");
     // [K: R blocks x HG heads][V: the same]
     static constexpr int STAGE_BYTES = 2 * R * HG * TILE_BYTES;
-    static constexpr int STAGE_BUDGET = PA_DECODE_STAGE_KIB * 1024;
+    static constexpr int STAGE_BUDGET = stage_budget_kib(D, B) * 1024;
     // At least 4 stages, unless a 4-stage ring of very large tiles would
     // exceed twice the budget (D 256 x B 32: 128 KiB, one CTA per SM); then
     // 3 stages, so that two CTAs fit (0.91 -> 0.985 of the copy rate there,

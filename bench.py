@@ -392,13 +392,15 @@ SIDE_WORKLOADS = ("tiny", "llama7b_b64", "cb_mix", "shared_prefix", "long_ctx", 
                   "cb_mix_4k")
 SIDE_SHARED = ("shared_prefix", "shared_prefix_4k")
 SIDE_MIN_SECONDS = 0.25
+SIDE_GRAPH = 20                 # decode launches per captured graph
 
 
 def side_workloads(args, dev):
     """The other decode workloads, timed in the same run as the step line:
     each workload's decode alone (its block tables and lengths, q and caches
-    drawn on the device), back to back between two events, at least
-    ROOFLINE_MIN_LAUNCHES launches and SIDE_MIN_SECONDS; then the
+    drawn on the device), back to back between two events from a replayed
+    CUDA graph of SIDE_GRAPH launches, at least ROOFLINE_MIN_LAUNCHES
+    launches and SIDE_MIN_SECONDS; then the
     shared-prefix call against pa_decode on each shared-prefix batch, one call
     per L2 flush.  Fractions are of the measured HBM copy rate."""
     import torch
@@ -444,20 +446,32 @@ def side_workloads(args, dev):
         fn = decode_fn(case, d)
         for _ in range(3):
             fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(10):
-            fn()
-        e1.record(stream)
         torch.cuda.synchronize(dev)
-        est = e0.elapsed_time(e1) / 10
-        n = min(200000, max(ROOFLINE_MIN_LAUNCHES, int(SIDE_MIN_SECONDS * 1e3 / max(est, 1e-3)) + 1))
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
+        # SIDE_GRAPH launches captured once and replayed, so that the host's
+        # per-call cost does not pace small batches
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(SIDE_GRAPH):
+                fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        est = e0.elapsed_time(e1) / SIDE_GRAPH
+        n = max(ROOFLINE_MIN_LAUNCHES, int(SIDE_MIN_SECONDS * 1e3 / max(est, 1e-3)) + 1)
+        reps = min(20000, (n + SIDE_GRAPH - 1) // SIDE_GRAPH)
+        n = reps * SIDE_GRAPH
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / n
+        del graph
         if pa.device_errors(stream=stream):
             raise RuntimeError(f"device error in the {w} decode")
         alg = workloads.decode_algorithmic_bytes(case)
@@ -522,10 +536,10 @@ def side_workloads(args, dev):
     if sampler:
         time.sleep(0.1)
         sampler.stop()
-    return {"method": "decode alone: back-to-back launches between two events (at least "
-                      f"{ROOFLINE_MIN_LAUNCHES} and {SIDE_MIN_SECONDS} s), inputs larger than L2 "
-                      "except tiny (whose launches are paced by the host's Python calls, not the "
-                      "GPU); shared-prefix call and pa_decode on its batch: one call per "
+    return {"method": "decode alone: back-to-back launches between two events, replayed from "
+                      f"a CUDA graph of {SIDE_GRAPH} launches (at least {ROOFLINE_MIN_LAUNCHES} "
+                      f"launches and {SIDE_MIN_SECONDS} s), inputs larger than L2 except tiny; "
+                      "shared-prefix call and pa_decode on its batch: one call per "
                       "L2 flush (256 MiB write, then 256 MiB read), mean over the calls; q and "
                       "caches drawn on the device; fractions of the measured HBM copy rate",
             "dtype": args.dtype, "results": res,

@@ -278,6 +278,25 @@ __device__ __forceinline__ float dot8(const uint4 kv, const uint4 qh, const floa
 #endif
 }
 
+// The lazily raised softmax reference may lag the running maximum by up to
+// this much (log2 units): weights stay at most 2^8 before a rescale.
+constexpr float kLazyLog2 = 8.f;
+
+// Lanes holding copies of the same row after consume_tile's reduce-scatter.
+template <int D, int B>
+__host__ __device__ constexpr int row_copies() {
+    using C = Cfg<D, B>;
+    return C::LPT >> ilog2(C::RG < C::LPT ? C::RG : C::LPT);
+}
+
+// The warp's sum of a per-lane row quantity (each row counted once).
+template <int D, int B>
+__device__ __forceinline__ float warp_row_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= row_copies<D, B>(); o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
 // One KV tile of one unit, processed by one warp.
 template <typename E, int D, int B>
 __device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t *vtile,
@@ -324,33 +343,39 @@ __device__ __forceinline__ void consume_tile(const uint8_t *ktile, const uint8_t
         for (int j = 0; j < V; ++j) sc[j] += __shfl_xor_sync(kFull, sc[j], o);
     }
 
-    // scale into the log2 domain, mask the tokens past the context, tile max
-    float tile_max = -INFINITY;
+    // scale into the log2 domain, mask the tokens past the context
+    float lane_max = -INFINITY;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int t = (base + j) * C::TPR + tr;
         sc[j] = (t < nvalid) ? sc[j] * scale_log2 : -INFINITY;
-        tile_max = fmaxf(tile_max, sc[j]);
+        lane_max = fmaxf(lane_max, sc[j]);
     }
-#pragma unroll
-    for (int o = 16; o >= DUP; o >>= 1)
-        tile_max = fmaxf(tile_max, __shfl_xor_sync(kFull, tile_max, o));
 
-    // online softmax update
-    const float new_max = fmaxf(run_max, tile_max);
-    const float alpha = exp2f(run_max - new_max);
-    float psum = 0.f;
+    // Online softmax with a lazily raised reference.  The weights are taken
+    // against run_max while no score of the tile exceeds it by more than
+    // kLazyLog2 (so no weight exceeds 2^kLazyLog2); only a tile that does
+    // reduces its maximum across the warp and rescales the state.  Every
+    // weight and the sum share one reference, so the normalised result is
+    // the same.  run_sum holds this lane's rows only; warp_row_sum adds the
+    // lanes up once the unit is done.
+    if (__any_sync(kFull, lane_max > run_max + kLazyLog2)) {
+        float tile_max = lane_max;
+#pragma unroll
+        for (int o = 16; o >= DUP; o >>= 1)
+            tile_max = fmaxf(tile_max, __shfl_xor_sync(kFull, tile_max, o));
+        const float new_max = fmaxf(run_max, tile_max);
+        const float alpha = exp2f(run_max - new_max);
+        run_sum *= alpha;
+#pragma unroll
+        for (int i = 0; i < C::DPL; ++i) acc[i] *= alpha;
+        run_max = new_max;
+    }
 #pragma unroll
     for (int j = 0; j < V; ++j) {
-        sc[j] = exp2f(sc[j] - new_max);
-        psum += sc[j];
+        sc[j] = exp2f(sc[j] - run_max);
+        run_sum += sc[j];
     }
-#pragma unroll
-    for (int o = 16; o >= DUP; o >>= 1) psum += __shfl_xor_sync(kFull, psum, o);
-    run_sum = run_sum * alpha + psum;
-    run_max = new_max;
-#pragma unroll
-    for (int i = 0; i < C::DPL; ++i) acc[i] *= alpha;
 
     // publish the B probabilities to the whole warp (one writer per token)
     if ((c & (DUP - 1)) == 0) {
@@ -1065,6 +1090,7 @@ __global__ void __launch_bounds__(Cfg<D, B, HG>::THREADS, Cfg<D, B, HG>::MIN_BLO
 
         // hand this warp's state to the unit's owner warp
         store_f32<C::DPL>(merge_acc + (slot * C::NC + w) * D + lane * C::DPL, acc);
+        run_sum = warp_row_sum<D, B>(run_sum);
         if (lane == 0) merge_ml[slot * C::NC + w] = make_float2(run_max, run_sum);
         __syncwarp();
         if (lane == 0) mbar_arrive(&merge_full[slot]);

@@ -102,6 +102,67 @@ def test_head_group_units_full_size(dev, D, B):
     assert_parity(got, oracle.decode_case(case), f"D={D} B={B} 64 heads")
 
 
+def _shape_scores(case, profile, rng):
+    """Rewrite every context token's K row so that its score against its
+    sequence's query follows `profile`: K_t = c_t * q + small noise, whose
+    score is about c_t |q|^2 * scale.  The oracle sees the same (rounded)
+    rows.  rising: over the last 8 tiles each tile's scores exceed the
+    previous maximum by about 12 (log2), past the lazy reference's margin of
+    8, so every such tile raises it; spike: one late token dwarfs the rest;
+    falling:
+    the first tile holds the maximum; saw: tiles alternate high and low."""
+    from gpu_helpers import as_float64
+    k = as_float64(case.k_cache, case.dtype).astype(np.float32)
+    q = as_float64(case.q, case.dtype).astype(np.float32)
+    B = case.block_size
+    for s, ctx in enumerate(case.context_lens):
+        ctx = int(ctx)
+        if ctx == 0:
+            continue
+        t = np.arange(ctx)
+        if profile == "rising":
+            # over the last 8 tiles, each tile about 12 (log2) above the one
+            # before: |q|^2 ~ D, so a score is about c sqrt(D) log2(e)
+            r = 12.0 / (B * np.sqrt(case.head_dim) * np.log2(np.e))
+            c = np.maximum(0, t - (ctx - 8 * B)) * r
+        elif profile == "spike":
+            c = np.full(ctx, 0.05)
+            c[int(rng.integers(ctx // 2, ctx))] = 3.0
+        elif profile == "falling":
+            c = 2.0 * (1.0 - t / ctx)
+        else:  # saw
+            c = np.where((t // B) % 2 == 0, 1.5, -0.5)
+        for h in range(case.num_heads):
+            rows = c[:, None] * q[s, h][None, :] + 0.05 * rng.standard_normal(
+                (ctx, case.head_dim), dtype=np.float32)
+            blocks = case.block_tables[s, t // B]
+            k[blocks, h, t % B, :] = rows
+    if case.dtype == "bf16":
+        case.k_cache[...] = workloads.f32_to_bf16_bits(k)
+    else:
+        case.k_cache[...] = k.astype(np.float16)
+
+
+@pytest.mark.parametrize("profile", ["rising", "spike", "falling", "saw"])
+@pytest.mark.parametrize("D,B", [(64, 8), (64, 16), (128, 16), (256, 32)])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_softmax_reference_profiles(dev, profile, D, B, dtype):
+    """Score profiles that drive the lazily raised softmax reference through
+    every path: a raise on every tile, one late raise, none after the first
+    tile, and alternating tiles; whole contexts and split ones (partials with
+    different references, combined)."""
+    rng = np.random.default_rng(41)
+    H = 4 if D == 64 else 2
+    case = _ragged(f"prof_{profile}", [1, 9, 40, 300, 700, 1500], H=H, D=D, B=B, seed=43,
+                   dtype=dtype)
+    _shape_scores(case, profile, rng)
+    ref = oracle.decode_case(case)
+    for P in (0, 4 * B):
+        got, flags, _ = run_gpu(case, dev, P)
+        assert flags == 0
+        assert_parity(got, ref, f"{profile} D={D} B={B} {dtype} P={P}", dtype=dtype)
+
+
 def test_split_matches_single_pass(dev):
     rng = np.random.default_rng(17)
     case = _ragged("split", rng.integers(1, 3000, size=24), H=8)

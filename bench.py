@@ -377,13 +377,35 @@ def config_of(case, args):
                    if getattr(args, "flush_l2", False) else
                    "inputs larger than L2 (no flush)" if 2 * case.k_cache.nbytes > L2_BYTES
                    else "inputs smaller than L2"),
-            "parallelism": f"dp{args.gpus} (replicas)", "seed": case.seed}
+            "parallelism": f"dp{args.gpus} (replicas)", "seed": case.seed,
+            "launch": ("eager, events around every step" if getattr(args, "flush_l2", False) else
+                       f"timed steps replayed from CUDA graphs of up to {STEP_GRAPH} steps, "
+                       "captured and uploaded during the warm-up")}
 
 
 # ----------------------------------------------------------------------------
 # native leg
 # ----------------------------------------------------------------------------
 
+STEP_GRAPH = 64                 # timed steps per captured CUDA graph
+
+
+def upload_graphs(graphs, stream):
+    """Upload captured graphs to the device (cuGraphUpload) ahead of their
+    first replay, so that the timed region does not pay for it; nothing runs.
+    Skipped where this torch does not expose the executable graph."""
+    import ctypes
+    try:
+        cuda = ctypes.CDLL("libcuda.so.1")
+        execs = [g.raw_cuda_graph_exec() for g in graphs]
+    except (OSError, AttributeError, RuntimeError):
+        return False
+    cuda.cuGraphUpload.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    cuda.cuGraphUpload.restype = ctypes.c_int
+    ok = all(cuda.cuGraphUpload(ctypes.c_void_p(e), ctypes.c_void_p(stream.cuda_stream)) == 0
+             for e in execs)
+    stream.synchronize()
+    return ok
 ROOFLINE_MIN_LAUNCHES = 200     # decode-only launches timed for the roofline
 ROOFLINE_MIN_SECONDS = 0.5      # ... and at least this long, so the clock sampler sees it
 
@@ -605,15 +627,35 @@ def run_native(args, rank, world, local_rank):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    for _ in range(max(3, args.warmup)):
+    # The first warm-up step runs the library's per-device set-up outside any
+    # capture; the timed steps' graphs are captured and uploaded (nothing
+    # runs) after it, so that the remaining warm-up steps lead straight into
+    # the timed region with no idle GPU in between.
+    step(d)
+    torch.cuda.synchronize(dev)
+    graphs = []
+    if not args.flush_l2:
+        left = args.steps
+        while left > 0:
+            n = min(left, STEP_GRAPH)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n):
+                    step(d)
+            graphs.append(g)
+            left -= n
+        upload_graphs(graphs, stream)
+    for _ in range(max(3, args.warmup) - 1):
         step(d)
     torch.cuda.synchronize(dev)
     if pa.device_errors(stream=stream):
         raise RuntimeError("device error during warm-up")
 
     # With --flush-l2 every step carries events around its kernels (the step
-    # time is built from them, flush excluded); otherwise the K steps run with
-    # no event between their kernels, so each decode may launch early.
+    # time is built from them, flush excluded).  Otherwise the K steps are
+    # replayed from the CUDA graphs captured above (up to STEP_GRAPH steps
+    # each), with no event between their kernels, so each decode may launch
+    # early behind its reshape_and_cache and one host call submits many steps.
     evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
            for _ in range(args.steps)] if args.flush_l2 else [None] * args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -622,10 +664,16 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t_begin = time.time()
     start.record(stream)
-    for i in range(args.steps):
-        step(d, evs[i])
+    if graphs:
+        with torch.cuda.stream(stream):
+            for g in graphs:
+                g.replay()
+    else:
+        for i in range(args.steps):
+            step(d, evs[i])
     end.record(stream)
     torch.cuda.synchronize(dev)
+    del graphs
     step_ms = start.elapsed_time(end) / args.steps
     if args.flush_l2:  # per-step events around reshape + decode, flush excluded
         step_ms = sum(e[2].elapsed_time(e[1]) for e in evs) / args.steps

@@ -7,7 +7,8 @@ and decodes.  After every step the output is compared with the oracle run on a
 host mirror of the cache that receives the same copies and writes.  The loop
 runs eagerly and replayed from a CUDA graph, with plain decode and with the
 shared-prefix decode (the batch ordered so that sharers are adjacent, the
-groups taken from the manager's sharing records every step), and pipelined:
+groups taken from the manager's sharing records every step), in fp16 and
+bf16, and pipelined:
 two staging slots in turn, each step's upload on a copy stream overlapping the
 previous step, and each step's output read after the next one is submitted."""
 import numpy as np
@@ -35,25 +36,46 @@ def dev():
     return d
 
 
-def _normal(rng, shape):
-    return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+def _normal(rng, shape, dtype="f16"):
+    x = rng.standard_normal(shape, dtype=np.float32)
+    return workloads.f32_to_bf16_bits(x) if dtype == "bf16" else x.astype(np.float16)
 
 
-@pytest.mark.parametrize("use_graph,host_out,shared,pipelined",
-                         [(False, False, False, False), (True, False, False, False),
-                          (True, True, False, False), (False, False, True, False),
-                          (True, False, True, False), (True, True, False, True),
-                          (False, False, True, True)])
-def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined):
+def _to_dev(a, dev):
+    """Host fp16 values or bf16 bit patterns -> a device tensor of that type."""
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def _to_host(t):
+    """A device fp16 tensor -> float16 values; bf16 -> uint16 bit patterns."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+@pytest.mark.parametrize("use_graph,host_out,shared,pipelined,dtype",
+                         [(False, False, False, False, "f16"), (True, False, False, False, "f16"),
+                          (True, True, False, False, "f16"), (False, False, True, False, "f16"),
+                          (True, False, True, False, "f16"), (True, True, False, True, "f16"),
+                          (False, False, True, True, "f16"), (True, True, False, True, "bf16"),
+                          (False, False, True, False, "bf16")])
+def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined, dtype):
     import torch
     import paged_kv_cache_269_gb300 as pa
     from paged_kv_cache_269_gb300.step import DecodeStep, PipelinedDecodeStep
     rng = np.random.default_rng(77 + use_graph)
     mgr = pa.KVManager(N, B, MB, shuffle_seed=5)
-    mirror_k = np.full((N, H, B, D), np.nan, np.float16)
-    mirror_v = np.full_like(mirror_k, np.nan)
-    kc = torch.from_numpy(mirror_k).to(dev)
-    vc = torch.from_numpy(mirror_v).to(dev)
+    if dtype == "bf16":   # NaN bit patterns in every slot not yet written
+        mirror_k = np.full((N, H, B, D), 0x7FC0, np.uint16)
+    else:
+        mirror_k = np.full((N, H, B, D), np.nan, np.float16)
+    mirror_v = mirror_k.copy()
+    kc = _to_dev(mirror_k, dev)
+    vc = _to_dev(mirror_v, dev)
     scale = float(np.float32(1 / np.sqrt(D)))
     # pipelined: two staging slots, step k + 1's upload overlapping step k,
     # each output checked after the next step has been submitted
@@ -67,8 +89,8 @@ def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined):
         if not pipelined:
             step.stream.synchronize()
         assert out.is_cuda != host_out              # the pinned host copy with host_out
-        assert_parity(out[:n].cpu().numpy(), ref, label)
-        assert (out[n:].cpu().numpy() == 0).all()          # padding rows
+        assert_parity(_to_host(out[:n]), ref, label, dtype=dtype)
+        assert (_to_host(out[n:]) == 0).all()              # padding rows
     grouped_steps = 0
 
     def write(slots, k, v):
@@ -77,15 +99,15 @@ def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined):
         slots = np.asarray(slots, np.int32)
         with torch.cuda.stream(step.stream):     # ordered with the steps
             ts = torch.from_numpy(slots).to(dev)
-            pa.reshape_and_cache(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), kc, vc,
-                                 ts)
+            pa.reshape_and_cache(_to_dev(k, dev), _to_dev(v, dev), kc, vc, ts)
         mirror_k, mirror_v = oracle.reshape_and_cache(k, v, mirror_k, mirror_v, slots)
 
     def prefill(seq, first):
         n = mgr.context_len(seq)
         if n > first:
             slots = [mgr.slot(seq, t) for t in range(first, n)]
-            write(slots, _normal(rng, (n - first, H, D)), _normal(rng, (n - first, H, D)))
+            write(slots, _normal(rng, (n - first, H, D), dtype),
+                  _normal(rng, (n - first, H, D), dtype))
 
     running = []
     system = mgr.add_sequence(80)                 # a 5-block system prompt
@@ -127,7 +149,7 @@ def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined):
             mirror_k, mirror_v = oracle.copy_blocks(mirror_k, mirror_v, mirror_k, mirror_v,
                                                     np.asarray(cow, np.int32))
         n = len(batch)
-        q, kn, vn = (_normal(rng, (n, H, D)) for _ in range(3))
+        q, kn, vn = (_normal(rng, (n, H, D), dtype) for _ in range(3))
         tables, lens = mgr.block_tables(batch, MB)
         groups = mgr.prefix_groups(batch, SMAX) if shared else None
         if shared and (groups[1] > 0).any():
@@ -140,9 +162,9 @@ def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined):
             ticket = it
         mirror_k, mirror_v = oracle.reshape_and_cache(kn, vn, mirror_k, mirror_v,
                                                       np.asarray(slots, np.int32))
-        ref = oracle.decode(q, mirror_k, mirror_v, tables, lens, scale)
+        ref = oracle.decode(q, mirror_k, mirror_v, tables, lens, scale, dtype=dtype)
         pending.append((ticket, n, ref, f"step {it} (graph={use_graph}, shared={shared}, "
-                                        f"pipelined={pipelined})"))
+                                        f"pipelined={pipelined}, {dtype})"))
         # a pipelined step's output is read once the next step is in flight
         while len(pending) > (1 if pipelined else 0):
             check(*pending.pop(0))
@@ -151,4 +173,4 @@ def test_continuous_batching_loop(dev, use_graph, host_out, shared, pipelined):
     assert pa.device_errors(stream=step.stream) == 0
     if shared:
         assert grouped_steps >= 20                         # the prefix path was exercised
-    assert np.array_equal(kc.cpu().numpy().view(np.uint16), mirror_k.view(np.uint16))
+    assert np.array_equal(_to_host(kc).view(np.uint16), mirror_k.view(np.uint16))
